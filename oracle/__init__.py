@@ -1,0 +1,220 @@
+"""CPU oracle for the fused sublayer boundary -- test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package. The CUDA
+library and its Python binding never touch it, and it shares no code with them.
+
+The arithmetic lives in ``oracle.c`` (plain single-threaded C, built with
+``-ffp-contract=off``); this file compiles it with gcc and marshals numpy /
+torch CPU buffers into it. Row ranges may be handed to several Python threads
+(ctypes drops the GIL during the call); each call stays single-threaded C.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_SO = os.path.join(_HERE, "liboracle.so")
+# A test may point the loader at another build of oracle.c (a planted-mistake copy)
+_SO_OVERRIDE = os.environ.get("BEAM_ORACLE_SO")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` beside its source with gcc."""
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    tmp = f"{_SO}.{os.getpid()}.tmp"
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+                    "-std=c11", _SRC, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if _SO_OVERRIDE:
+                lib = ctypes.CDLL(_SO_OVERRIDE)
+            else:
+                build()
+                lib = ctypes.CDLL(_SO)
+            vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+            ld = ctypes.c_longdouble
+            lib.oracle_bf16_rne.argtypes = [f32]
+            lib.oracle_bf16_rne.restype = ctypes.c_uint16
+            lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_f32.restype = f32
+            lib.oracle_sum_f32_exact.argtypes = [vp, i64]
+            lib.oracle_sum_f32_exact.restype = f32
+            lib.oracle_sum_squares.argtypes = [vp, i32]
+            lib.oracle_sum_squares.restype = f32
+            lib.oracle_rms_factor.argtypes = [f32, i32, f32]
+            lib.oracle_rms_factor.restype = f32
+            lib.oracle_rmsnorm.argtypes = [vp, vp, f32, i32, vp]
+            lib.oracle_rmsnorm.restype = None
+            lib.oracle_scales.argtypes = [i32, vp, vp]
+            lib.oracle_scales.restype = None
+            lib.oracle_moe_combine.argtypes = [vp, vp, i32, i32, vp]
+            lib.oracle_moe_combine.restype = None
+            lib.oracle_boundary.argtypes = [vp, vp, vp, vp, i32, f32, i64, i32, vp]
+            lib.oracle_boundary.restype = i32
+            lib.oracle_moe_boundary.argtypes = [vp, vp, vp, i32, vp, vp, i32, f32, i64, i32, vp]
+            lib.oracle_moe_boundary.restype = i32
+            lib.oracle_boundary_ld.argtypes = [vp, vp, vp, vp, i32, ld, i64, i32, vp]
+            lib.oracle_boundary_ld.restype = i32
+            lib.oracle_residual_ld.argtypes = [vp, vp, i32, i64]
+            lib.oracle_residual_ld.restype = None
+            _lib = lib
+    return _lib
+
+
+# ---------------------------------------------------------------- marshalling
+
+def as_u16(a) -> np.ndarray:
+    """BF16 bit patterns as a C-contiguous uint16 numpy array (torch bf16 or uint16 input)."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            assert a.dtype == torch.bfloat16 and a.device.type == "cpu"
+            return a.contiguous().view(torch.int16).numpy().view(np.uint16)
+    except ImportError:
+        pass
+    a = np.asarray(a)
+    assert a.dtype == np.uint16
+    return np.ascontiguousarray(a)
+
+
+def _p(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def bf16_rne(f: float) -> int:
+    return int(_load().oracle_bf16_rne(float(f)))
+
+
+def bf16_to_f32(b: int) -> float:
+    return float(_load().oracle_bf16_to_f32(int(b)))
+
+
+def sum_f32_exact(t) -> float:
+    t = np.ascontiguousarray(t, dtype=np.float32)
+    return float(_load().oracle_sum_f32_exact(_p(t), t.size))
+
+
+def sum_squares(v) -> float:
+    v = as_u16(v)
+    return float(_load().oracle_sum_squares(_p(v), v.size))
+
+
+def rms_factor(S: float, D: int, eps: float) -> float:
+    return float(_load().oracle_rms_factor(S, D, eps))
+
+
+def rmsnorm(v, w, eps: float) -> np.ndarray:
+    v, w = as_u16(v), as_u16(w)
+    out = np.empty_like(v)
+    _load().oracle_rmsnorm(_p(v), _p(w), eps, v.size, _p(out))
+    return out
+
+
+def scales(n: int) -> tuple[float, float]:
+    c1, c2 = ctypes.c_float(), ctypes.c_float()
+    _load().oracle_scales(n, ctypes.byref(c1), ctypes.byref(c2))
+    return c1.value, c2.value
+
+
+def moe_combine(e, w) -> np.ndarray:
+    e = as_u16(e)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    K, D = e.shape
+    out = np.empty(D, np.uint16)
+    _load().oracle_moe_combine(_p(e), _p(w), K, D, _p(out))
+    return out
+
+
+def _row_split(T: int, threads: int):
+    threads = max(1, min(threads, T))
+    step = -(-T // threads) if T else 0
+    return [(r, min(T, r + step)) for r in range(0, T, step)] if T else []
+
+
+def boundary(h, x, post_w, pre_w, n: int, eps: float, threads: int = 1):
+    """Dense boundary; returns (h', y) as uint16 arrays [T, D] (inputs are not modified)."""
+    h = as_u16(h).copy()
+    x, post_w, pre_w = as_u16(x), as_u16(post_w), as_u16(pre_w)
+    T, D = h.shape
+    y = np.empty_like(h)
+    lib = _load()
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        rc = lib.oracle_boundary(_p(h[lo:hi]), _p(x[lo:hi]), _p(post_w), _p(pre_w), n, eps,
+                                 hi - lo, D, _p(y[lo:hi]))
+        if rc != 0:
+            raise ValueError("oracle_boundary: bad arguments")
+
+    _run_rows(run, T, threads)
+    return h, y
+
+
+def moe_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: float, threads: int = 1):
+    """MoE combine + boundary; returns (h', y) as uint16 arrays [T, D]."""
+    h = as_u16(h).copy()
+    e = as_u16(expert_out)
+    w = np.ascontiguousarray(topk_w.numpy() if hasattr(topk_w, "numpy") else topk_w,
+                             dtype=np.float32)
+    post_w, pre_w = as_u16(post_w), as_u16(pre_w)
+    T, K, D = e.shape
+    y = np.empty_like(h)
+    lib = _load()
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        rc = lib.oracle_moe_boundary(_p(h[lo:hi]), _p(e[lo:hi]), _p(w[lo:hi]), K, _p(post_w),
+                                     _p(pre_w), n, eps, hi - lo, D, _p(y[lo:hi]))
+        if rc != 0:
+            raise ValueError("oracle_moe_boundary: bad arguments")
+
+    _run_rows(run, T, threads)
+    return h, y
+
+
+def _run_rows(fn, T: int, threads: int):
+    parts = _row_split(T, threads)
+    if len(parts) <= 1:
+        for p in parts:
+            fn(p)
+        return
+    with ThreadPoolExecutor(len(parts)) as ex:
+        list(ex.map(fn, parts))
+
+
+def boundary_ld(h, x, post_w, pre_w, n: int, eps: float):
+    """The boundary in long double with no rounding; numpy longdouble arrays in, (h', y) out."""
+    h = np.array(h, dtype=np.longdouble, order="C")
+    x = np.ascontiguousarray(x, dtype=np.longdouble)
+    post_w = np.ascontiguousarray(post_w, dtype=np.longdouble)
+    pre_w = np.ascontiguousarray(pre_w, dtype=np.longdouble)
+    T, D = h.shape
+    y = np.empty_like(h)
+    rc = _load().oracle_boundary_ld(_p(h), _p(x), _p(post_w), _p(pre_w), n, eps, T, D, _p(y))
+    if rc != 0:
+        raise ValueError("oracle_boundary_ld: bad arguments")
+    return h, y
+
+
+def residual_ld(h, x, n: int) -> np.ndarray:
+    h = np.array(h, dtype=np.longdouble, order="C")
+    x = np.ascontiguousarray(x, dtype=np.longdouble)
+    _load().oracle_residual_ld(_p(h), _p(x), n, h.size)
+    return h

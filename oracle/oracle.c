@@ -1,0 +1,282 @@
+/*
+ * CPU oracle for the fused sublayer boundary of the Beam decoder.
+ *
+ * TEST INFRASTRUCTURE ONLY. The tests, the package's smoke check and the
+ * bench's CPU-baseline leg are the only callers. The CUDA library never links,
+ * loads or calls this file, and this file shares no code with it.
+ *
+ * What it computes (one token row at a time, plain loops, one thread):
+ *
+ *   Sandwich norm and depth-scaled residual (Beam blog, SGLang page,
+ *   "Sandwich normalization and depth-scaled residual"; vLLM page, "MoE and
+ *   residual stream"): every branch has an input and an output RMSNorm, and
+ *   the n-th residual add is  h <- sqrt((n-1)/n) * h + x / sqrt(n).
+ *   Both scaled operands are rounded to the activation dtype (BF16) before the
+ *   add (SGLang page, same section). The fused boundary keeps FP32 math and
+ *   the BF16 rounding points of the unfused code (vLLM page, "Agent-driven
+ *   optimization", change 1), and the unfused code writes the normalised
+ *   branch (SGLang page, same section), so that branch is a BF16 tensor.
+ *
+ *   RMSNorm, FP32 math (the pages give no formula; the standard RMS norm):
+ *     S   = RN32( sum_j RN32(v_j * v_j) )   exact sum, rounded once
+ *     ms  = RN32(S / D)
+ *     r   = RN32(1 / RN32(sqrt(RN32(ms + eps))))
+ *     out = bf16( RN32( RN32(v_j * r) * w_j ) )
+ *   The pages leave the order of the FP32 sum open and accept FP32
+ *   reduction-order differences as noise (SGLang page, "BF16 MoE kernel
+ *   optimization" and "Reinforcement learning in Miles"); the oracle takes the
+ *   one order-free FP32 value, the exact sum rounded once to nearest-even.
+ *
+ *   Boundary, per row:
+ *     xn_j = rmsnorm(x, post_w)_j                      (BF16)
+ *     c1   = RN32(sqrt((n-1)/n)), c2 = RN32(1/sqrt(n))  (evaluated in double)
+ *     a_j  = bf16(RN32(c1 * h_j)),  b_j = bf16(RN32(c2 * xn_j))
+ *     h'_j = bf16(RN32(a_j + b_j))                     (stored over h)
+ *     y_j  = rmsnorm(h', pre_w)_j                      (BF16)
+ *
+ *   MoE combine in front of the boundary (vLLM page, change 3: after the MoE
+ *   the norm kernel also combines the top-8 expert outputs; SGLang page,
+ *   "Fusion optimizations": the BF16 MoE path folds the local expert sum,
+ *   the routing scale and the BF16 rounding together; "Dense layers and
+ *   grouped MoE routing": FP32 routing coefficients):
+ *     acc_j = 0; for k = 0..K-1: acc_j = fma(w_k, e_kj, acc_j)   (FP32)
+ *     x_j   = bf16(acc_j)
+ *   The routing scale of 2.5 is already inside w.
+ *
+ * bf16(v) is IEEE-754 round-to-nearest-even from FP32 to the 8-bit
+ * significand; any NaN becomes the quiet NaN 0x7FFF; overflow gives +-inf;
+ * subnormals are kept. Build with -ffp-contract=off so that no mul+add pair is
+ * fused behind the source's back.
+ *
+ * The *_ld functions repeat the boundary in long double with no rounding at
+ * all; they exist for the hand-worked and closed-form checks.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef uint16_t bf16_t;
+
+static float f32_of_bits(uint32_t u) {
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint32_t bits_of_f32(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return u;
+}
+
+float oracle_bf16_to_f32(bf16_t b) { return f32_of_bits((uint32_t)b << 16); }
+
+bf16_t oracle_bf16_rne(float f) {
+    uint32_t u = bits_of_f32(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0) return 0x7FFF;
+    uint32_t keep = u >> 16;      /* sign, exponent and the top 7 fraction bits */
+    uint32_t rest = u & 0xFFFFu;  /* the 16 dropped bits */
+    /* above the halfway point, or exactly halfway with an odd kept part: round the
+     * magnitude up; a carry out of the fraction correctly bumps the exponent,
+     * up to infinity */
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1;
+    return (bf16_t)keep;
+}
+
+/* ------------------------------------------------------------------------
+ * Exact sum of non-negative floats, rounded once to FP32.
+ *
+ * A finite float t >= 0 with biased exponent field E and fraction f is
+ * m * 2^(q - 149) with m = (E ? 2^23 + f : f) < 2^24 and q = (E ? E - 1 : 0).
+ * The sum is held exactly as the integer N = sum m * 2^q in a little-endian
+ * array of single bits; the value is N * 2^-149. 320 bits hold 2^43 terms.
+ * ---------------------------------------------------------------------- */
+#define ACC_BITS 320
+
+typedef struct {
+    uint8_t bit[ACC_BITS];
+    int any_nan, any_inf, any_negative;
+} exact_acc;
+
+static void acc_init(exact_acc* a) { memset(a, 0, sizeof *a); }
+
+static void acc_add(exact_acc* a, float t) {
+    uint32_t u = bits_of_f32(t);
+    uint32_t E = (u >> 23) & 0xFFu, f = u & 0x7FFFFFu;
+    if (E == 0xFFu) {
+        if (f) a->any_nan = 1;
+        else if (u >> 31) a->any_negative = 1;
+        else a->any_inf = 1;
+        return;
+    }
+    if ((u >> 31) && (u & 0x7FFFFFFFu)) { a->any_negative = 1; return; }
+    uint32_t m = E ? (f | 0x800000u) : f;
+    int q = E ? (int)E - 1 : 0;
+    for (int i = 0; i < 24; ++i) {
+        if (!((m >> i) & 1u)) continue;
+        int p = q + i; /* add 2^p with carry */
+        while (a->bit[p]) a->bit[p++] = 0;
+        a->bit[p] = 1;
+    }
+}
+
+static float acc_round(const exact_acc* a) {
+    if (a->any_nan || a->any_negative) return NAN;
+    if (a->any_inf) return INFINITY;
+    int top = -1;
+    for (int p = ACC_BITS - 1; p >= 0; --p)
+        if (a->bit[p]) { top = p; break; }
+    if (top < 0) return 0.0f;
+    if (top <= 23) {
+        /* N < 2^24: N * 2^-149 is a subnormal or lies in the first normal
+         * binade; either way it is exact and its bit pattern is N itself */
+        uint32_t v = 0;
+        for (int p = top; p >= 0; --p) v = (v << 1) | a->bit[p];
+        return f32_of_bits(v);
+    }
+    int lo = top - 23; /* keep bits lo..top (24 bits) */
+    uint32_t m = 0;
+    for (int p = top; p >= lo; --p) m = (m << 1) | a->bit[p];
+    int half = a->bit[lo - 1], sticky = 0;
+    for (int p = lo - 2; p >= 0; --p) sticky |= a->bit[p];
+    if (half && (sticky || (m & 1u))) m += 1;
+    if (m == (1u << 24)) { m >>= 1; lo += 1; }
+    /* value = m * 2^(lo - 149) with m in [2^23, 2^24): biased exponent lo + 1 */
+    uint32_t Eb = (uint32_t)lo + 1u;
+    if (Eb >= 255u) return INFINITY;
+    return f32_of_bits((Eb << 23) | (m & 0x7FFFFFu));
+}
+
+/* RN32 of the exact sum of t[0..n-1]; every t must be >= 0 (else NaN) */
+float oracle_sum_f32_exact(const float* t, int64_t n) {
+    exact_acc* a = (exact_acc*)malloc(sizeof(exact_acc));
+    if (!a) return NAN;
+    acc_init(a);
+    for (int64_t i = 0; i < n; ++i) acc_add(a, t[i]);
+    float s = acc_round(a);
+    free(a);
+    return s;
+}
+
+/* S = RN32(sum_j RN32(v_j * v_j)) over a BF16 row */
+float oracle_sum_squares(const bf16_t* v, int D) {
+    exact_acc a;
+    acc_init(&a);
+    for (int j = 0; j < D; ++j) {
+        float vj = oracle_bf16_to_f32(v[j]);
+        float sq = vj * vj;
+        acc_add(&a, sq);
+    }
+    return acc_round(&a);
+}
+
+/* r = 1 / sqrt(S / D + eps), each operation in FP32 */
+float oracle_rms_factor(float S, int D, float eps) {
+    float ms = S / (float)D;
+    float v = ms + eps;
+    float root = sqrtf(v);
+    return 1.0f / root;
+}
+
+/* out_j = bf16((v_j * r) * w_j), r from the row's mean square */
+void oracle_rmsnorm(const bf16_t* v, const bf16_t* w, float eps, int D, bf16_t* out) {
+    float r = oracle_rms_factor(oracle_sum_squares(v, D), D, eps);
+    for (int j = 0; j < D; ++j) {
+        float p = oracle_bf16_to_f32(v[j]) * r;
+        float q = p * oracle_bf16_to_f32(w[j]);
+        out[j] = oracle_bf16_rne(q);
+    }
+}
+
+/* depth-scaled residual coefficients for the n-th add (n >= 1) */
+void oracle_scales(int n, float* c1, float* c2) {
+    *c1 = (float)sqrt((double)(n - 1) / (double)n);
+    *c2 = (float)(1.0 / sqrt((double)n));
+}
+
+/* x_j = bf16(fma chain over k of w_k * e_kj), e is [K, D], w is [K] */
+void oracle_moe_combine(const bf16_t* e, const float* w, int K, int D, bf16_t* x_out) {
+    for (int j = 0; j < D; ++j) {
+        float acc = 0.0f;
+        for (int k = 0; k < K; ++k) acc = fmaf(w[k], oracle_bf16_to_f32(e[(int64_t)k * D + j]), acc);
+        x_out[j] = oracle_bf16_rne(acc);
+    }
+}
+
+/* one row of the boundary given its (BF16) branch output x */
+static void boundary_row(bf16_t* h, const bf16_t* x, const bf16_t* post_w, const bf16_t* pre_w,
+                         float c1, float c2, float eps, int D, bf16_t* y, bf16_t* xn) {
+    oracle_rmsnorm(x, post_w, eps, D, xn);
+    for (int j = 0; j < D; ++j) {
+        float a = oracle_bf16_to_f32(oracle_bf16_rne(c1 * oracle_bf16_to_f32(h[j])));
+        float b = oracle_bf16_to_f32(oracle_bf16_rne(c2 * oracle_bf16_to_f32(xn[j])));
+        h[j] = oracle_bf16_rne(a + b);
+    }
+    oracle_rmsnorm(h, pre_w, eps, D, y);
+}
+
+/* Dense boundary. h [T,D] in/out; x, y [T,D]; post_w, pre_w [D]. Returns 0, or -1 on bad sizes. */
+int oracle_boundary(bf16_t* h, const bf16_t* x, const bf16_t* post_w, const bf16_t* pre_w, int n,
+                    float eps, int64_t T, int D, bf16_t* y) {
+    if (n < 1 || D < 1 || T < 0) return -1;
+    float c1, c2;
+    oracle_scales(n, &c1, &c2);
+    bf16_t* xn = (bf16_t*)malloc(sizeof(bf16_t) * (size_t)D);
+    if (!xn) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        boundary_row(h + t * D, x + t * D, post_w, pre_w, c1, c2, eps, D, y + t * D, xn);
+    free(xn);
+    return 0;
+}
+
+/* MoE boundary. e [T,K,D]; topk_w [T,K] FP32; other operands as the dense boundary. */
+int oracle_moe_boundary(bf16_t* h, const bf16_t* e, const float* topk_w, int K,
+                        const bf16_t* post_w, const bf16_t* pre_w, int n, float eps, int64_t T,
+                        int D, bf16_t* y) {
+    if (n < 1 || D < 1 || T < 0 || K < 1) return -1;
+    float c1, c2;
+    oracle_scales(n, &c1, &c2);
+    bf16_t* x = (bf16_t*)malloc(sizeof(bf16_t) * (size_t)D * 2);
+    if (!x) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        oracle_moe_combine(e + t * (int64_t)K * D, topk_w + t * K, K, D, x);
+        boundary_row(h + t * D, x, post_w, pre_w, c1, c2, eps, D, y + t * D, x + D);
+    }
+    free(x);
+    return 0;
+}
+
+/* ---- long double, no rounding anywhere ----------------------------------- */
+
+static void rmsnorm_ld(const long double* v, const long double* w, long double eps, int D,
+                       long double* out) {
+    long double s = 0.0L;
+    for (int j = 0; j < D; ++j) s += v[j] * v[j];
+    long double r = 1.0L / sqrtl(s / (long double)D + eps);
+    for (int j = 0; j < D; ++j) out[j] = v[j] * r * w[j];
+}
+
+int oracle_boundary_ld(long double* h, const long double* x, const long double* post_w,
+                       const long double* pre_w, int n, long double eps, int64_t T, int D,
+                       long double* y) {
+    if (n < 1 || D < 1 || T < 0) return -1;
+    long double c1 = sqrtl((long double)(n - 1) / (long double)n);
+    long double c2 = 1.0L / sqrtl((long double)n);
+    long double* xn = (long double*)malloc(sizeof(long double) * (size_t)D);
+    if (!xn) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        rmsnorm_ld(x + t * D, post_w, eps, D, xn);
+        for (int j = 0; j < D; ++j) h[t * D + j] = c1 * h[t * D + j] + c2 * xn[j];
+        rmsnorm_ld(h + t * D, pre_w, eps, D, y + t * D);
+    }
+    free(xn);
+    return 0;
+}
+
+/* residual update alone, long double: h <- sqrt((n-1)/n) h + x / sqrt(n) */
+void oracle_residual_ld(long double* h, const long double* x, int n, int64_t count) {
+    long double c1 = sqrtl((long double)(n - 1) / (long double)n);
+    long double c2 = 1.0L / sqrtl((long double)n);
+    for (int64_t i = 0; i < count; ++i) h[i] = c1 * h[i] + c2 * x[i];
+}

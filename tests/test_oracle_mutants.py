@@ -1,0 +1,92 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case below plants one mistake in a copy of ``oracle/oracle.c`` (on the
+CPU, in a temporary directory), builds it, and runs the pin suite
+``test_oracle_pins.py`` against that build. Every planted mistake must make at
+least one pin fail.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+# (name, text in oracle.c, replacement)
+MUTANTS = [
+    ("residual coefficients swapped",
+     "oracle_bf16_rne(c1 * oracle_bf16_to_f32(h[j]))", "oracle_bf16_rne(c2 * oracle_bf16_to_f32(h[j]))"),
+    ("scaled stream not rounded to BF16",
+     "float a = oracle_bf16_to_f32(oracle_bf16_rne(c1 * oracle_bf16_to_f32(h[j])));",
+     "float a = c1 * oracle_bf16_to_f32(h[j]);"),
+    ("scaled branch not rounded to BF16",
+     "float b = oracle_bf16_to_f32(oracle_bf16_rne(c2 * oracle_bf16_to_f32(xn[j])));",
+     "float b = c2 * oracle_bf16_to_f32(xn[j]);"),
+    ("post-norm uses the pre-norm weight",
+     "oracle_rmsnorm(x, post_w, eps, D, xn);", "oracle_rmsnorm(x, pre_w, eps, D, xn);"),
+    ("next pre-norm reads the branch instead of the new stream",
+     "oracle_rmsnorm(h, pre_w, eps, D, y);", "oracle_rmsnorm(x, pre_w, eps, D, y);"),
+    ("mean over D - 1", "float ms = S / (float)D;", "float ms = S / (float)(D - 1);"),
+    ("eps dropped", "float v = ms + eps;", "float v = ms;"),
+    ("c1 without the square root",
+     "*c1 = (float)sqrt((double)(n - 1) / (double)n);", "*c1 = (float)((double)(n - 1) / (double)n);"),
+    ("c2 = 1/n", "*c2 = (float)(1.0 / sqrt((double)n));", "*c2 = (float)(1.0 / (double)n);"),
+    ("BF16 ties rounded away from zero",
+     "(rest == 0x8000u && (keep & 1u))", "(rest == 0x8000u)"),
+    ("BF16 rounding truncates", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1;",
+     "if (0) keep += 1;"),
+    ("sum rounding ignores ties-to-even", "if (half && (sticky || (m & 1u))) m += 1;",
+     "if (half) m += 1;"),
+    ("sum rounding drops the sticky bits", "if (half && (sticky || (m & 1u))) m += 1;",
+     "if (half && (m & 1u)) m += 1;"),
+    ("weight applied before the rms factor",
+     "float p = oracle_bf16_to_f32(v[j]) * r;\n        float q = p * oracle_bf16_to_f32(w[j]);",
+     "float p = oracle_bf16_to_f32(v[j]) * oracle_bf16_to_f32(w[j]);\n        float q = p * r;"),
+    ("MoE running sum rounded to BF16 per expert",
+     "acc = fmaf(w[k], oracle_bf16_to_f32(e[(int64_t)k * D + j]), acc);",
+     "acc = oracle_bf16_to_f32(oracle_bf16_rne(fmaf(w[k], oracle_bf16_to_f32(e[(int64_t)k * D + j]), acc)));"),
+    ("MoE product and add rounded separately",
+     "acc = fmaf(w[k], oracle_bf16_to_f32(e[(int64_t)k * D + j]), acc);",
+     "acc = acc + w[k] * oracle_bf16_to_f32(e[(int64_t)k * D + j]);"),
+    ("MoE experts combined in reverse order",
+     "for (int k = 0; k < K; ++k) acc = fmaf(", "for (int k = K - 1; k >= 0; --k) acc = fmaf("),
+    ("MoE uses the first routing weight for every expert", "fmaf(w[k],", "fmaf(w[0],"),
+    ("MoE expert row index dropped", "e[(int64_t)k * D + j]", "e[(int64_t)k + j]"),
+    ("long-double residual coefficient squared",
+     "long double c1 = sqrtl((long double)(n - 1) / (long double)n);\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i",
+     "long double c1 = (long double)(n - 1) / (long double)n;\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i"),
+]
+
+
+def _run_mutant(case, tmp):
+    name, old, new = case
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site not found: {name}"
+    mutated = src.replace(old, new)
+    tag = "".join(c if c.isalnum() else "_" for c in name)
+    c_path = os.path.join(tmp, f"{tag}.c")
+    so_path = os.path.join(tmp, f"{tag}.so")
+    with open(c_path, "w") as f:
+        f.write(mutated)
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-std=c11", c_path,
+                    "-o", so_path, "-lm"], check=True)
+    env = dict(os.environ, BEAM_ORACLE_SO=so_path)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    return name, r.returncode
+
+
+@pytest.mark.slow
+def test_every_planted_mistake_fails_a_pin():
+    with tempfile.TemporaryDirectory() as tmp:
+        with ThreadPoolExecutor(max(1, min(8, os.cpu_count() or 1))) as ex:
+            results = list(ex.map(lambda c: _run_mutant(c, tmp), MUTANTS))
+    survivors = [name for name, rc in results if rc == 0]
+    assert not survivors, f"mistakes no pin caught: {survivors}"

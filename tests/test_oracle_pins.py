@@ -1,0 +1,502 @@
+"""Pins for the CPU oracle, checked against things other than the oracle itself.
+
+Each test ties one part of the oracle to a library routine (torch's BF16 cast,
+IEEE float32 arithmetic in numpy), to exact rational arithmetic, to a closed
+form of the depth-scaled residual, to an invariant the pages state, or to the
+hand-worked examples in ``tests/golden/hand_examples.txt``.
+"""
+from __future__ import annotations
+
+import math
+import os
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_examples.txt")
+f32 = np.float32
+
+
+# ----------------------------------------------------------------- helpers
+
+def bf16_bits(vals) -> np.ndarray:
+    """BF16 bit patterns of FP32 values via torch's cast (a library routine)."""
+    t = torch.tensor(np.asarray(vals, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f32(b) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)
+
+
+def nearest_f32(q: Fraction) -> np.float32:
+    """The FP32 value nearest to the rational q, ties to even (brute force on neighbours)."""
+    if q == 0:
+        return f32(0.0)
+    c = f32(float(q)) if abs(q) < Fraction(2) ** 128 else f32(np.inf)
+    best = None
+    cands = {c, np.nextafter(c, f32(np.inf)), np.nextafter(c, f32(-np.inf))}
+    for v in cands:
+        if not np.isfinite(v):
+            continue
+        d = abs(Fraction(float(v)) - q)
+        key = (d, int(np.array(v).view(np.uint32)) & 1)  # ties: even significand first
+        if best is None or key < best[0]:
+            best = (key, v)
+    # beyond the largest finite float by at least half an ulp -> infinity
+    fmax = Fraction(float(np.finfo(np.float32).max))
+    half_ulp = Fraction(2) ** (127 - 24)
+    if q >= fmax + half_ulp:
+        return f32(np.inf)
+    return best[1]
+
+
+def exact_sum(vals) -> Fraction:
+    return sum((Fraction(float(v)) for v in vals), Fraction(0))
+
+
+def load_golden():
+    ex = {}
+    for line in open(GOLDEN):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        key, val = line.split(":", 1)
+        name, field = key.split(".")
+        vals = [float(v) for v in val.split()]
+        ex.setdefault(name, {})[field] = vals if field in (
+            "h", "x", "post_w", "pre_w", "h_out", "y") else vals[0]
+    return ex
+
+
+# ------------------------------------------------------------- BF16 rounding
+
+def test_bf16_rne_matches_torch_cast_on_random_bit_patterns():
+    rng = np.random.default_rng(123)
+    u = rng.integers(0, 2**32, size=20000, dtype=np.uint64).astype(np.uint32)
+    vals = u.view(np.float32)
+    want = bf16_bits(vals)
+    got = np.array([oracle.bf16_rne(float(v)) for v in vals], dtype=np.uint16)
+    nan = np.isnan(vals)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert all(((g & 0x7F80) == 0x7F80) and (g & 0x7F) for g in got[nan])
+
+
+def test_bf16_rne_ties_subnormals_and_overflow():
+    cases = []
+    for hi in (0x3F80, 0x3F81, 0x0001, 0x0002, 0x807F, 0x7F7F, 0xFF7F, 0x0080):
+        for lo in (0x7FFF, 0x8000, 0x8001, 0x0000, 0xFFFF):
+            cases.append(np.uint32((hi << 16) | lo))
+    vals = np.array(cases, dtype=np.uint32).view(np.float32)
+    want = bf16_bits(vals)
+    got = np.array([oracle.bf16_rne(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, want)
+    assert oracle.bf16_rne(float("inf")) == 0x7F80
+    assert oracle.bf16_rne(float("-inf")) == 0xFF80
+
+
+# -------------------------------------------------- exact sum, rounded once
+
+@pytest.mark.parametrize("seed", range(6))
+def test_exact_sum_is_nearest_float_of_rational_sum(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 400))
+    # spread exponents widely, include subnormals and zeros
+    mant = rng.random(n).astype(np.float32)
+    expo = rng.integers(-150, 40, size=n)
+    t = np.ldexp(mant, expo).astype(np.float32)
+    t[rng.random(n) < 0.05] = 0.0
+    got = oracle.sum_f32_exact(t)
+    assert f32(got) == nearest_f32(exact_sum(t))
+
+
+def test_exact_sum_ties_go_to_even():
+    one, e24, e40 = 1.0, 2.0 ** -24, 2.0 ** -40
+    # 1 + 2^-24 is the midpoint of 1 and 1 + 2^-23: ties to the even one, 1
+    assert oracle.sum_f32_exact([one, e24]) == 1.0
+    # a tiny extra term breaks the tie upwards
+    assert oracle.sum_f32_exact([one, e24, e40]) == 1.0 + 2.0 ** -23
+    # (1 + 2^-23) + 2^-24 is a midpoint with an odd lower neighbour: rounds up
+    assert oracle.sum_f32_exact([1.0 + 2.0 ** -23, e24]) == 1.0 + 2.0 ** -22
+    # many tiny terms that together pass the midpoint
+    assert oracle.sum_f32_exact([one] + [2.0 ** -30] * 65) == 1.0 + 2.0 ** -23
+
+
+def test_exact_sum_subnormal_exact_and_overflow():
+    tiny = float(np.array(1, np.uint32).view(np.float32))  # 2^-149
+    assert oracle.sum_f32_exact([tiny] * 7) == 7 * tiny
+    assert oracle.sum_f32_exact([2.0 ** -126 - tiny, tiny]) == 2.0 ** -126
+    big = float(f32(1.5 * 2.0 ** 127))
+    assert math.isinf(oracle.sum_f32_exact([big, big]))
+    assert math.isnan(oracle.sum_f32_exact([1.0, float("nan")]))
+    assert math.isinf(oracle.sum_f32_exact([1.0, float("inf")]))
+    assert oracle.sum_f32_exact([]) == 0.0
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_sum_squares_uses_fp32_products_and_one_rounding(seed):
+    rng = np.random.default_rng(100 + seed)
+    D = 257
+    v = rng.standard_normal(D).astype(np.float32) * np.float32(2.0) ** rng.integers(-70, 10, D)
+    b = bf16_bits(v)
+    xf = bits_to_f32(b)
+    sq = xf * xf  # numpy float32 products: IEEE RN, subnormals kept
+    assert f32(oracle.sum_squares(b)) == nearest_f32(exact_sum(sq))
+
+
+def test_rms_factor_matches_ieee_float32_steps():
+    rng = np.random.default_rng(7)
+    for _ in range(2000):
+        S = f32(rng.random() * 10.0 ** int(rng.integers(-3, 6)))
+        D = int(rng.integers(1, 9000))
+        eps = f32([0.0, 1e-6, 1e-5][rng.integers(0, 3)])
+        want = f32(1.0) / np.sqrt(S / f32(D) + eps)
+        assert f32(oracle.rms_factor(float(S), D, float(eps))) == want
+
+
+# -------------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_single_element_closed_form():
+    rng = np.random.default_rng(11)
+    for _ in range(500):
+        x = f32(rng.standard_normal() * 4)
+        w = f32(1 + 0.1 * rng.standard_normal())
+        xb, wb = bf16_bits([x])[0], bf16_bits([w])[0]
+        xf, wf = bits_to_f32([xb])[0], bits_to_f32([wb])[0]
+        r = f32(1.0) / np.sqrt(xf * xf + f32(1e-6))
+        want = bf16_bits([(xf * r) * wf])[0]
+        got = oracle.rmsnorm(np.array([xb], np.uint16), np.array([wb], np.uint16), 1e-6)[0]
+        assert got == want
+
+
+@pytest.mark.parametrize("k", [-20, -3, 1, 9])
+def test_rmsnorm_is_invariant_to_power_of_two_scaling_with_zero_eps(k):
+    rng = np.random.default_rng(5)
+    D = 640
+    x = bf16_bits(rng.standard_normal(D))
+    w = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    xs = bf16_bits(bits_to_f32(x) * f32(2.0 ** k))  # exact scaling
+    assert np.array_equal(oracle.rmsnorm(x, w, 0.0), oracle.rmsnorm(xs, w, 0.0))
+
+
+def test_rmsnorm_unit_weights_give_unit_rms_and_weights_multiply():
+    rng = np.random.default_rng(6)
+    D = 5120
+    x = bf16_bits(rng.standard_normal(D) * 3.7)
+    ones = bf16_bits(np.ones(D))
+    y = bits_to_f32(oracle.rmsnorm(x, ones, 1e-6)).astype(np.float64)
+    assert abs(np.mean(y * y) - 1.0) < 2.0 ** -9
+    twos = bf16_bits(np.full(D, 2.0))
+    y2 = bits_to_f32(oracle.rmsnorm(x, twos, 1e-6))
+    assert np.array_equal(y2, (2 * y).astype(np.float32))
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_rmsnorm_matches_torch_cpu_composition(seed):
+    """Independent restatement: exact rational sum, then torch float32 ops and torch's BF16 cast."""
+    rng = np.random.default_rng(40 + seed)
+    D = 1024
+    x = bf16_bits(rng.standard_normal(D))
+    w = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    xt = torch.from_numpy(bits_to_f32(x).copy())
+    wt = torch.from_numpy(bits_to_f32(w).copy())
+    S = nearest_f32(exact_sum((xt * xt).numpy()))
+    # numpy's float32 sqrt is IEEE correctly rounded; torch's CPU sqrt is not always
+    r = torch.tensor(f32(1.0) / np.sqrt(S / f32(D) + f32(1e-6)))
+    want = ((xt * r) * wt).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.rmsnorm(x, w, 1e-6), want)
+
+
+def _nearest_f32_of_fsum(vals: np.ndarray) -> np.float32:
+    """RN32 of the exact sum: fsum gives the correctly rounded double; if that double
+    is exactly halfway between two floats the exact rational decides."""
+    d = math.fsum(vals.astype(np.float64).tolist())
+    c = f32(d)
+    lo, hi = np.nextafter(c, f32(-np.inf)), np.nextafter(c, f32(np.inf))
+    if d in ((float(c) + float(lo)) / 2, (float(c) + float(hi)) / 2):
+        return nearest_f32(exact_sum(vals))
+    return c
+
+
+def test_rmsnorm_matches_torch_cpu_composition_on_a_million_elements():
+    """Order of the two FP32 products, (v r) w, shows in about one element per
+    million, so this cross-check runs on 256 rows of 5120."""
+    rng = np.random.default_rng(44)
+    T, D = 256, 5120
+    x = bf16_bits(rng.standard_normal((T, D)))
+    w = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    xt = torch.from_numpy(bits_to_f32(x).copy())
+    wt = torch.from_numpy(bits_to_f32(w).copy())
+    sq = (xt * xt).numpy()
+    S = np.array([_nearest_f32_of_fsum(sq[t]) for t in range(T)], np.float32).reshape(T, 1)
+    r = torch.from_numpy(f32(1.0) / np.sqrt(S / f32(D) + f32(1e-6)))
+    want = ((xt * r) * wt).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.stack([oracle.rmsnorm(x[t], w, 1e-6) for t in range(T)])
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------ depth-scaled residual
+
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 20, 104, 105, 1000])
+def test_scales_are_rounded_sqrt_and_keep_unit_variance(n):
+    c1, c2 = oracle.scales(n)
+    getcontext().prec = 50
+    t1 = (Decimal(n - 1) / Decimal(n)).sqrt()
+    t2 = 1 / Decimal(n).sqrt()
+    for c, t in ((c1, t1), (c2, t2)):
+        c = f32(c)
+        ulp = float(np.spacing(c)) if c != 0 else 2.0 ** -149
+        assert abs(Decimal(float(c)) - t) <= Decimal(ulp)
+    # (sqrt((n-1)/n))^2 + (1/sqrt(n))^2 = 1 up to the FP32 rounding of c1, c2
+    assert abs(float(c1) ** 2 + float(c2) ** 2 - 1.0) < 2.0 ** -22
+
+
+def test_n1_makes_the_stream_the_normalised_branch():
+    rng = np.random.default_rng(9)
+    T, D = 3, 520
+    h = bf16_bits(rng.standard_normal((T, D)))
+    x = bf16_bits(rng.standard_normal((T, D)))
+    pw = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    qw = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    h2, y = oracle.boundary(h, x, pw, qw, 1, 1e-6)
+    for t in range(T):
+        xn = oracle.rmsnorm(x[t], pw, 1e-6)
+        assert np.array_equal(np.abs(bits_to_f32(h2[t])), np.abs(bits_to_f32(xn)))
+        assert np.array_equal(h2[t] & 0x7FFF, xn & 0x7FFF)
+        assert np.array_equal(y[t], oracle.rmsnorm(h2[t], qw, 1e-6))
+
+
+def test_post_and_pre_weights_are_not_swapped():
+    # D = 1, n = 1 (c1 = 0, c2 = 1): h' = bf16(x r1 w_post), y = bf16(h' r2 w_pre)
+    one = bf16_bits([1.0])
+    h2, y = oracle.boundary(bf16_bits([[0.0]]), bf16_bits([[1.0]]), bf16_bits([2.0]),
+                            bf16_bits([0.5]), 1, 1e-6)
+    assert bits_to_f32(h2)[0, 0] == 2.0 and bits_to_f32(y)[0, 0] == 0.5
+    h2s, ys = oracle.boundary(bf16_bits([[0.0]]), bf16_bits([[1.0]]), bf16_bits([0.5]),
+                              bf16_bits([2.0]), 1, 1e-6)
+    assert bits_to_f32(h2s)[0, 0] == 0.5 and bits_to_f32(ys)[0, 0] == 2.0
+    assert one[0] == 0x3F80
+
+
+@pytest.mark.parametrize("name", ["A", "B", "C"])
+def test_hand_worked_examples(name):
+    ex = load_golden()[name]
+    D = int(ex["D"])
+    h = bf16_bits([ex["h"]])
+    x = bf16_bits([ex["x"]])
+    h2, y = oracle.boundary(h, x, bf16_bits(ex["post_w"]), bf16_bits(ex["pre_w"]), int(ex["n"]),
+                            float(ex["eps"]))
+    assert h2.shape == (1, D)
+    assert np.array_equal(bits_to_f32(h2)[0], np.array(ex["h_out"], np.float32))
+    if "y" in ex:
+        assert np.array_equal(bits_to_f32(y)[0], np.array(ex["y"], np.float32))
+
+
+def test_long_double_residual_chain_closed_form():
+    """Applying n = 2..N to h1 gives (h1 + sum_n x_n) / sqrt(N): the products of
+    sqrt((j-1)/j) telescope to sqrt(k/N)."""
+    rng = np.random.default_rng(21)
+    N, M = 105, 64
+    h1 = rng.standard_normal(M)
+    xs = rng.standard_normal((N - 1, M))
+    h = np.array(h1, dtype=np.longdouble)
+    for n in range(2, N + 1):
+        h = oracle.residual_ld(h, xs[n - 2], n)
+    closed = (h1.astype(np.longdouble) + xs.astype(np.longdouble).sum(0)) / np.sqrt(
+        np.longdouble(N))
+    assert np.max(np.abs(h - closed)) < 1e-14
+
+
+def test_long_double_boundary_matches_bf16_oracle_within_rounding():
+    rng = np.random.default_rng(22)
+    T, D = 4, 512
+    hb = bf16_bits(rng.standard_normal((T, D)))
+    xb = bf16_bits(rng.standard_normal((T, D)))
+    pw = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    qw = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    n = 9
+    h2, y = oracle.boundary(hb, xb, pw, qw, n, 1e-6)
+    hl, yl = oracle.boundary_ld(bits_to_f32(hb), bits_to_f32(xb), bits_to_f32(pw),
+                                bits_to_f32(qw), n, 1e-6)
+    hl, yl = hl.astype(np.float64), yl.astype(np.float64)
+    h0 = bits_to_f32(hb).astype(np.float64)
+    xf = bits_to_f32(xb).astype(np.float64)
+    xn_ld = xf / np.sqrt(np.mean(xf * xf, 1, keepdims=True) + 1e-6) * bits_to_f32(pw)
+    c1, c2 = math.sqrt((n - 1) / n), 1 / math.sqrt(n)
+    # BF16 keeps 8 significant bits (unit roundoff 2^-8): each of xn, a, b, h' is off by
+    # at most 2^-8 relative, so h' is off by at most 2^-8 (|c1 h| + 2 |c2 xn| + |h'|)
+    # (cancellation in a + b makes this absolute, not relative to h')
+    dh = np.abs(bits_to_f32(h2) - hl)
+    bound_h = 2.0 ** -8 * (np.abs(c1 * h0) + 2 * np.abs(c2 * xn_ld) + np.abs(hl)) * 1.01 + 1e-7
+    assert (dh <= bound_h).all()
+    # y = h' r2 w: carries h''s error, r2's relative error and its own rounding
+    qwf = bits_to_f32(qw).astype(np.float64)
+    r2 = 1 / np.sqrt(np.mean(hl * hl, 1, keepdims=True) + 1e-6)
+    dy = np.abs(bits_to_f32(y) - yl)
+    bound_y = bound_h * r2 * np.abs(qwf) + 2.0 ** -7 * np.abs(yl) + 1e-7
+    assert np.mean(dh) < 0.25 * np.mean(bound_h)  # typical error well inside the bound
+    assert (dy <= bound_y).all()
+
+
+def _chain(T, D, steps, seed, weights_fixed=False):
+    rng = np.random.default_rng(seed)
+    h1 = bf16_bits(rng.standard_normal((T, D)))
+    h = h1.copy()
+    xn_sum = np.zeros((T, D), np.longdouble)
+    xn_sq = 0.0
+    for s in range(steps):
+        n = s + 2
+        x = bf16_bits(rng.standard_normal((T, D)))
+        pw = bf16_bits(np.ones(D) if weights_fixed else 1 + 0.1 * rng.standard_normal(D))
+        qw = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+        xn = np.stack([oracle.rmsnorm(x[t], pw, 1e-6) for t in range(T)])
+        xnf = bits_to_f32(xn).astype(np.float64)
+        xn_sum += xnf
+        xn_sq += np.mean(xnf * xnf)
+        h, _ = oracle.boundary(h, x, pw, qw, n, 1e-6)
+    return h1, h, xn_sum, xn_sq
+
+
+def test_bf16_chain_follows_closed_form_of_depth_scaling():
+    T, D, steps = 2, 512, 104
+    h1, h, xn_sum, _ = _chain(T, D, steps, 31)
+    closed = (bits_to_f32(h1).astype(np.longdouble) + xn_sum) / np.sqrt(np.longdouble(steps + 1))
+    got = bits_to_f32(h).astype(np.float64)
+    rel_rms = np.sqrt(np.mean((got - closed.astype(np.float64)) ** 2) /
+                      np.mean(closed.astype(np.float64) ** 2))
+    # 104 steps of three BF16 roundings each, damped by the depth scaling
+    assert rel_rms < 0.03
+
+
+def test_chain_keeps_unit_variance_statistically():
+    """sqrt((n-1)/n)^2 + (1/sqrt(n))^2 = 1: with unit-variance h and branches the
+    stream keeps unit variance; here the prediction uses the data's own branch
+    second moments: var(h_N) = (var(h_1) + sum_n mean(xn_n^2)) / N."""
+    T, D, steps = 8, 5120, 104
+    h1, h, _, xn_sq = _chain(T, D, steps, 32)
+    h1f = bits_to_f32(h1).astype(np.float64)
+    pred = (np.mean(h1f * h1f) + xn_sq) / (steps + 1)
+    got = np.mean(bits_to_f32(h).astype(np.float64) ** 2)
+    sigma = math.sqrt(2.0 / (T * D))
+    assert abs(got - pred) < 5 * sigma
+    assert abs(pred - 1.0099) < 0.02  # E[w^2] = 1.01 for weights 1 + 0.1 N(0,1)
+
+
+# --------------------------------------------------------------- MoE combine
+
+def test_moe_one_hot_weights_reduce_to_a_single_scaled_expert():
+    rng = np.random.default_rng(50)
+    K, D = 8, 256
+    e = bf16_bits(rng.standard_normal((K, D)))
+    for k in range(K):
+        w = np.zeros(K, np.float32)
+        w[k] = f32(rng.random() * 2.5)
+        want = bf16_bits(w[k] * bits_to_f32(e[k]))
+        assert np.array_equal(oracle.moe_combine(e, w), want)
+
+
+def test_moe_equal_experts_power_of_two_values_sum_exactly():
+    K, D = 8, 64
+    vals = np.float32(2.0) ** np.arange(-10, 54, dtype=np.float32)[:D] * np.where(
+        np.arange(D) % 2, 1, -1).astype(np.float32)
+    vals = np.clip(vals, -2.0 ** 100, 2.0 ** 100).astype(np.float32)
+    e = np.tile(bf16_bits(vals), (K, 1))
+    w = np.full(K, 2.5 / 8, np.float32)
+    got = bits_to_f32(oracle.moe_combine(e, w))
+    assert np.array_equal(got, (2.5 * bits_to_f32(e[0])).astype(np.float32))
+
+
+def test_moe_boundary_with_one_unit_expert_is_the_dense_boundary():
+    rng = np.random.default_rng(51)
+    T, D = 3, 384
+    h = bf16_bits(rng.standard_normal((T, D)))
+    x = bf16_bits(rng.standard_normal((T, D)))
+    pw = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    qw = bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    hd, yd = oracle.boundary(h, x, pw, qw, 5, 1e-6)
+    hm, ym = oracle.moe_boundary(h, x.reshape(T, 1, D), np.ones((T, 1), np.float32), pw, qw, 5,
+                                 1e-6)
+    assert np.array_equal(hd, hm) and np.array_equal(yd, ym)
+
+
+def _fma_chain_exact(e_bits: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """acc <- RN32(w_k e_k + acc) for k ascending, each step from the exact rational."""
+    ef = bits_to_f32(e_bits)
+    K, D = ef.shape
+    acc = [Fraction(0)] * D
+    for k in range(K):
+        wk = Fraction(float(w[k]))
+        acc = [Fraction(float(nearest_f32(wk * Fraction(float(ef[k, j])) + acc[j])))
+               for j in range(D)]
+    return bf16_bits([float(a) for a in acc])
+
+
+def test_moe_combine_is_an_fma_chain_in_expert_order():
+    """Each step is one rounding of w_k e_k + acc (exact rational, then RN32), k ascending."""
+    rng = np.random.default_rng(52)
+    K, D = 8, 512
+    e = bf16_bits(rng.standard_normal((K, D)))
+    w = (rng.random(K) * 0.6).astype(np.float32)
+    assert np.array_equal(oracle.moe_combine(e, w), _fma_chain_exact(e, w))
+
+
+def test_moe_combine_fused_multiply_add_decides_a_bf16_tie():
+    # w1 e1 = (1 + 2^-23)(1 + 2^-7) = 1 + 2^-7 + 2^-23 + 2^-30. Fused with acc = 1 the sum
+    # 2 + 2^-7 + 2^-23 + 2^-30 rounds up to 2 + 2^-7 + 2^-22, past the BF16 midpoint
+    # 2 + 2^-7, so x = 2 + 2^-6. Rounding the product first gives 2 + 2^-7 + 2^-23,
+    # an FP32 tie that goes to the even 2 + 2^-7, a BF16 tie that goes to 2.
+    e = bf16_bits([[1.0], [1.0078125]])
+    w = np.array([1.0, 1.0 + 2.0 ** -23], np.float32)
+    got = oracle.moe_combine(e, w)
+    assert bits_to_f32(got)[0] == 2.015625
+    assert np.array_equal(got, _fma_chain_exact(e, w))
+
+
+def test_moe_combine_order_decides_a_bf16_tie():
+    # 1, 2^-8, 2^-24, 2^-24 in this order: 1 + 2^-8, then two FP32 ties that stay at the
+    # even 1 + 2^-8, a BF16 tie -> 1. Summed from the last expert: 2^-23 + 2^-8 + 1 is
+    # exact and passes the BF16 midpoint -> 1 + 2^-7.
+    e = bf16_bits([[1.0], [2.0 ** -8], [2.0 ** -24], [2.0 ** -24]])
+    w = np.ones(4, np.float32)
+    got = oracle.moe_combine(e, w)
+    assert bits_to_f32(got)[0] == 1.0
+    assert np.array_equal(got, _fma_chain_exact(e, w))
+
+
+def test_moe_combine_rounds_once_after_the_fp32_sum():
+    # experts 1, 2^-8, 2^-8 with unit weights: the FP32 sum 1 + 2^-7 is a BF16 value.
+    # Rounding the running sum to BF16 after each expert would give 1 + 2^-8 -> 1
+    # (a tie, to even) and stay at 1.
+    e = bf16_bits([[1.0], [2.0 ** -8], [2.0 ** -8]])
+    got = bits_to_f32(oracle.moe_combine(e, np.array([1.0, 1.0, 1.0], np.float32)))
+    assert got[0] == 1.0078125
+
+
+# ------------------------------------------------------------ input generator
+
+def test_generator_is_counter_based_and_seeded():
+    a = synth.normal(3, 2, 1000)
+    b = synth.normal(3, 2, 400, start=600)
+    assert np.array_equal(a[600:], b)
+    assert not np.array_equal(a, synth.normal(4, 2, 1000))
+    assert not np.array_equal(a, synth.normal(3, 5, 1000))
+
+
+def test_generator_distributions():
+    z = synth.normal(0, 1, 400000).astype(np.float64)
+    assert abs(z.mean()) < 0.01 and abs(z.var() - 1) < 0.01
+    t = synth.student_t3_unit(0, 9, 400000).astype(np.float64)
+    assert abs(np.median(t)) < 0.01
+    # t3 / sqrt(3): P(|t| > 1) = P(|T3| > sqrt(3)) = 0.18165 (closed form of the t3 CDF)
+    p = np.mean(np.abs(t) > 1.0)
+    assert abs(p - 0.18165) < 0.004
+    w = synth.topk_weights(3, 6, 1000)
+    assert np.allclose(w.sum(1), 2.5, atol=1e-5) and (w > 0).all()
+    m = synth.bernoulli(4, 7, 200000, 1e-3)
+    assert 120 < m.sum() < 290
