@@ -1,0 +1,408 @@
+"""Benchmark of the fused sublayer boundary on GB300.
+
+One step = one decoder layer's two boundaries on a batch of T = 16384 tokens
+(8 x 2048 prefill), D = 5120: the attention boundary (dense, n = 7) and the
+MoE boundary (top-8 combine, n = 20). Together they run every step of the hot
+path (combine, post-norm, depth-scaled residual, pre-norm).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). `value` is tokens/s through the step, all ranks
+together (each rank has its own 16384-token batch: weak scaling, no
+data-path collective). `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+T_TOKENS = 16384
+D = 5120
+DENSE_N, MOE_N, EPS = 7, 20, 1e-6
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "fused boundary tokens/s at T=16384 (dense + MoE boundary of one decoder layer)"
+
+# DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), valid only for the kernel source it was taken on.
+NCU_TRAFFIC = {}  # kernel -> {"bytes_per_launch": B, "source_sha": sha, "profile": path}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sandwich_norm_residual_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dense_bytes(T: int) -> int:
+    return T * 8 * D + 4 * D           # read h, x; write h', y; two weight vectors
+
+
+def moe_bytes(T: int) -> int:
+    return T * (22 * D + 32) + 4 * D   # read 8 expert rows, 8 weights, h; write h', y
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a float over all ranks (one tiny all-reduce; identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def shard_rows(total: int, rank: int, world: int) -> tuple[int, int]:
+    """Contiguous row block of `rank` (used when a fixed batch is split across ranks)."""
+    per, rem = divmod(total, world)
+    lo = rank * per + min(rank, rem)
+    return lo, lo + per + (1 if rank < rem else 0)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.rows: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.t = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [r for (t, r) in self.rows if t0 <= t <= t1]
+        used = inside or [r for (t, r) in self.rows if t >= t0][:3]
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in used:
+            try:
+                mhz.append(float(r[1]))
+                mx = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        mhz.sort()
+        return {"sm_mhz": mhz[len(mhz) // 2] if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def measured_hbm_peak() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def make_inputs(device, pin: bool):
+    import torch
+    import synth
+    from synth import CONFIGS
+    dense_cfg, moe_cfg = CONFIGS[2], CONFIGS[3]
+    dn = synth.dense_inputs(dense_cfg)
+    mo = synth.moe_inputs(moe_cfg)
+    host = {"dense": dn, "moe": mo}
+    if pin:
+        host = {g: {k: v.pin_memory() for k, v in d.items()} for g, d in host.items()}
+    dev = {g: {k: v.to(device) for k, v in d.items()} for g, d in host.items()}
+    dev["dense"]["y"] = torch.empty_like(dev["dense"]["h"])
+    dev["moe"]["y"] = torch.empty_like(dev["moe"]["h"])
+    return host, dev
+
+
+def run_step(snr, d, stream):
+    dn, mo = d["dense"], d["moe"]
+    snr.boundary_fused(dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, y=dn["y"],
+                       stream=stream)
+    snr.moe_combine_boundary(mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"], mo["pre_w"],
+                             MOE_N, EPS, y=mo["y"], stream=stream)
+
+
+def bench_ours(args, rank, world, local_rank):
+    import torch
+    import sandwich_norm_residual_gb300 as snr
+    from sandwich_norm_residual_gb300 import build as libbuild
+
+    libbuild.build()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    stream = torch.cuda.Stream(device)
+    host, dev = make_inputs(device, pin=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            run_step(snr, dev, stream)
+    snr.sync_status(stream)
+
+    # per-kernel durations: events around each launch on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    try:
+        props = torch.cuda.get_device_properties(device)
+        uuid = str(getattr(props, "uuid", "") or "")
+        gpu_id = f"GPU-{uuid}" if uuid and not uuid.startswith("GPU-") else (uuid or None)
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        dn, mo = dev["dense"], dev["moe"]
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            snr.boundary_fused(dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS,
+                               y=dn["y"], stream=stream)
+            ev[i][1].record(stream)
+            snr.moe_combine_boundary(mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"],
+                                     mo["pre_w"], MOE_N, EPS, y=mo["y"], stream=stream)
+            ev[i][2].record(stream)
+        end.record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    barrier(device)
+    snr.sync_status(stream)
+    time.sleep(0.2)
+    sampler.stop()
+
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, device)
+    ms_step = ms_total / args.steps
+    dense_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    moe_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+
+    # end to end through the public API: pinned host inputs in, results out, every step
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    out_host = {g: {k: torch.empty_like(host[g]["h"], device="cpu").pin_memory() for k in ("h", "y")}
+                for g in ("dense", "moe")}
+    h2d = sum(v.numel() * v.element_size() for g in host.values() for v in g.values())
+    d2h = sum(v.numel() * v.element_size() for g in out_host.values() for v in g.values())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for g in ("dense", "moe"):
+                for k, v in host[g].items():
+                    dev[g][k].copy_(v, non_blocking=True)
+            run_step(snr, dev, stream)
+            for g in ("dense", "moe"):
+                for k in ("h", "y"):
+                    out_host[g][k].copy_(dev[g][k], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, device)
+    snr.sync_status(stream)
+
+    if rank != 0:
+        _finish(world)
+        return
+
+    peak, peak_kind = measured_hbm_peak()
+    db, mb = dense_bytes(T_TOKENS), moe_bytes(T_TOKENS)
+    dense_gbs = db / (dense_us * 1e-6) / 1e9
+    moe_gbs = mb / (moe_us * 1e-6) / 1e9
+    sha = kernel_source_sha()
+    tr = NCU_TRAFFIC.get("moe")
+    traffic = tr["bytes_per_launch"] if tr and tr.get("source_sha") == sha else None
+    clocks = sampler.summary(t0, t1)
+    line = {
+        "metric": METRIC,
+        "value": world * T_TOKENS / (ms_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"layer boundary pair, T={T_TOKENS} tokens per GPU, D={D}: dense "
+                        f"boundary n={DENSE_N} + MoE top-8 combine boundary n={MOE_N}, eps=1e-6; "
+                        "storage bf16, math fp32",
+            "T": T_TOKENS, "D": D,
+            "l2": "inputs larger than L2 (129 MB): no flush between steps",
+            "dense": {"us": dense_us, "tokens_per_s": T_TOKENS / (dense_us * 1e-6),
+                      "GBps": dense_gbs, "frac_of_measured_hbm": dense_gbs / peak,
+                      "frac_of_nominal_8TBps": dense_gbs / NOMINAL_HBM_GBS, "bytes": db},
+            "moe": {"us": moe_us, "tokens_per_s": T_TOKENS / (moe_us * 1e-6),
+                    "GBps": moe_gbs, "frac_of_measured_hbm": moe_gbs / peak,
+                    "frac_of_nominal_8TBps": moe_gbs / NOMINAL_HBM_GBS, "bytes": mb},
+            "kernel_source_sha": sha,
+            "parallelism": f"{world} independent replica(s), no collective on the data path",
+        },
+        "roofline": {"kernel": "moe_combine_boundary", "bound": "hbm", "achieved": moe_gbs,
+                     "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                     "frac": moe_gbs / peak, "traffic": traffic},
+        "e2e": {"value": world * T_TOKENS / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    _finish(world)
+
+
+def _finish(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def oracle_step_sample(rows: int, row0: int = 0):
+    """Inputs of `rows` tokens of the step's workload (both boundaries)."""
+    import synth
+    from synth import CONFIGS
+    return (synth.dense_inputs(CONFIGS[2], row_start=row0, rows=rows),
+            synth.moe_inputs(CONFIGS[3], row_start=row0, rows=rows))
+
+
+def oracle_step(dn, mo):
+    import oracle
+    oracle.boundary(dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, threads=1)
+    oracle.moe_boundary(mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"], mo["pre_w"], MOE_N,
+                        EPS, threads=1)
+
+
+def cpu_baseline(seconds: float) -> dict:
+    """The oracle, as it stands, on one host core, over a bounded sample of the workload."""
+    rows, done, spent = 16, 0, 0.0
+    while spent < seconds:
+        dn, mo = oracle_step_sample(rows, done % T_TOKENS)
+        t0 = time.perf_counter()
+        oracle_step(dn, mo)
+        spent += time.perf_counter() - t0
+        done += rows
+    return {"value": done / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of the {T_TOKENS} tokens through both boundaries, "
+                      f"{spent:.1f} s single-threaded C"}
+
+
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_step(*oracle_step_sample(rows))
+    spent = 0.0
+    for i in range(args.steps):
+        dn, mo = oracle_step_sample(rows, (i * rows) % T_TOKENS)
+        t0 = time.perf_counter()
+        oracle_step(dn, mo)
+        spent += time.perf_counter() - t0
+    value = args.steps * rows / spent
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spent / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"layer boundary pair, T={T_TOKENS}, D={D}: dense n={DENSE_N} + "
+                               f"MoE n={MOE_N}; each step a {rows}-token sample",
+                   "T": T_TOKENS, "D": D},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} tokens per step, {args.steps} steps"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-rows", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        bench_reference(args, rank, world)
+    else:
+        bench_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * libbeamboundary -- the fused sublayer boundary of the Beam decoder on one
+ * NVIDIA GB300 (sm_103a) GPU.
+ *
+ * At each of the decoder's 104 sublayer boundaries (52 layers x attention and
+ * feed-forward) three steps run as one kernel:
+ *
+ *   1. post-RMSNorm of the branch output x                     -> xn (BF16)
+ *   2. depth-scaled residual add, n-th add:
+ *        h <- bf16( bf16(c1 * h) + bf16(c2 * xn) ),
+ *        c1 = RN32(sqrt((n-1)/n)), c2 = RN32(1/sqrt(n))
+ *   3. pre-RMSNorm of the new stream for the next sublayer     -> y  (BF16)
+ *
+ * Sources (Beam blog pages):
+ *   - sandwich norm, an RMSNorm before and after every sublayer, and the
+ *     residual rule h <- sqrt((n-1)/n) h + x/sqrt(n): vLLM page, "MoE and
+ *     residual stream"; SGLang page, "Sandwich normalization and
+ *     depth-scaled residual" (which also states that both scaled operands
+ *     are rounded to the activation dtype before the add, and that the
+ *     unfused transition writes the normalised branch, reads it for the
+ *     residual combine and reads the result again for the next input norm);
+ *   - one fused kernel with FP32 math and the reference implementation's
+ *     BF16 rounding points: vLLM page, "Agent-driven optimization", change 1;
+ *   - the MoE variant, where the same norm kernel first combines the top-8
+ *     expert outputs: vLLM page, change 3; SGLang page, "Fusion
+ *     optimizations" (local expert sum, routing scale and BF16 rounding in
+ *     one path) and "Dense layers and grouped MoE routing" (FP32 routing
+ *     coefficients, the routing scale carried in the routing weights).
+ *
+ * Arithmetic, per token row, all FP32 with IEEE round-to-nearest-even:
+ *   RMSNorm(v, w)_j = bf16( (v_j * r) * w_j ),  r = 1 / sqrt(S/D + eps),
+ *   S = the exact sum of the FP32 squares v_j * v_j, rounded once to FP32.
+ *   The pages leave the summation order open and accept FP32 order
+ *   differences; this library returns the order-free value (an error-free
+ *   compensated sum whose rounding is certified per row, with an exact
+ *   integer fallback), so results do not depend on launch shape.
+ *   MoE: x_j = bf16(acc_j), acc_j = fma chain over k = 0..7 of w[t,k]*e[t,k,j].
+ *
+ * Data layout: every tensor is dense, row-major, token-major.
+ *   BF16 values are passed as their 16-bit patterns (uint16_t).
+ *   h, x, y_out:  [T, D]       expert_out: [T, 8, D]      topk_w: [T, 8] FP32
+ *   post_w, pre_w: [D]
+ * All pointers are DEVICE pointers on the current device (or managed memory).
+ * Every pointer must be 16-byte aligned; D must be a multiple of 8 with
+ * 8 <= D <= BEAM_MAX_D.
+ *
+ * Ownership: the caller owns every buffer. The library allocates no device or
+ * host memory in any call and keeps no per-call state. Per device it keeps a
+ * small status word and a counter in static device memory (see
+ * beam_sync_status).
+ *
+ * Streams: calls are asynchronous on the given stream (NULL = the legacy
+ * default stream). Calls may be made from several host threads.
+ *
+ * Errors: argument errors are returned before anything is launched and leave
+ * every buffer untouched. A failed launch returns BEAM_ERR_CUDA. Errors
+ * raised inside a kernel (a bounded wait that gave up) set the device status
+ * word, reported by beam_sync_status. No C++ exception crosses this ABI.
+ */
+#ifndef BEAM_BOUNDARY_H
+#define BEAM_BOUNDARY_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BEAM_API __attribute__((visibility("default")))
+#else
+#define BEAM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st* beam_stream_t;
+
+typedef enum {
+    BEAM_OK = 0,
+    BEAM_ERR_NULL = 1,    /* a required pointer is NULL (T > 0) */
+    BEAM_ERR_ALIGN = 2,   /* a pointer is not 16-byte aligned */
+    BEAM_ERR_SHAPE = 3,   /* T < 0, D not a multiple of 8, D < 8, D > BEAM_MAX_D, T*D too large */
+    BEAM_ERR_ARG = 4,     /* n < 1, or eps negative / not finite, or a bad option */
+    BEAM_ERR_ALIAS = 5,   /* y_out overlaps another operand, or h partly overlaps an input */
+    BEAM_ERR_CUDA = 6,    /* a CUDA runtime call failed (device query, launch, sync) */
+    BEAM_ERR_TIMEOUT = 7, /* a bounded device-side wait gave up (see beam_sync_status) */
+    BEAM_ERR_DEVICE = 8   /* the current device is not an sm_103 GPU */
+} beam_status;
+
+/* Largest supported hidden size. */
+#define BEAM_MAX_D 32768
+/* Experts combined per token by beam_moe_combine_boundary (top-8 routing). */
+#define BEAM_MOE_TOPK 8
+
+/*
+ * Dense boundary: post-RMSNorm of x, depth-scaled residual into h (in place),
+ * pre-RMSNorm of the new h into y_out.
+ *   h      [T, D] BF16, read and overwritten with h'
+ *   x      [T, D] BF16 branch output; may be the same pointer as h (then the
+ *          branch is the old stream); any other overlap with h is an error
+ *   post_w [D] BF16 weight of the post-norm; pre_w [D] BF16 weight of the
+ *          next sublayer's pre-norm
+ *   n      index of this residual add, n >= 1 (n = 1 makes h' = xn)
+ *   eps    RMSNorm epsilon, finite and >= 0
+ *   T      token rows (T = 0 returns BEAM_OK and launches nothing; the
+ *          pointers are then not checked)
+ *   y_out  [T, D] BF16, must not overlap h, x, post_w or pre_w
+ */
+BEAM_API beam_status beam_boundary_fused(beam_stream_t stream, uint16_t* h, const uint16_t* x,
+                                const uint16_t* post_w, const uint16_t* pre_w, int n, float eps,
+                                int64_t T, int D, uint16_t* y_out);
+
+/*
+ * MoE boundary: x = bf16(sum_k topk_w[t,k] * expert_out[t,k,:]) (FP32 fma
+ * chain, k ascending), then the dense boundary on that x.
+ *   expert_out [T, 8, D] BF16: the token's 8 routed expert outputs, contiguous
+ *   topk_w     [T, 8] FP32 routing weights with the routing scale (2.5 for
+ *              Beam) and renormalisation already applied
+ *   other arguments as beam_boundary_fused; y_out must not overlap h,
+ *   expert_out, topk_w or the weights, and h must not overlap expert_out.
+ */
+BEAM_API beam_status beam_moe_combine_boundary(beam_stream_t stream, uint16_t* h,
+                                      const uint16_t* expert_out, const float* topk_w,
+                                      const uint16_t* post_w, const uint16_t* pre_w, int n,
+                                      float eps, int64_t T, int D, uint16_t* y_out);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns BEAM_OK, BEAM_ERR_TIMEOUT if a kernel's bounded wait gave up
+ * since the last read, or BEAM_ERR_CUDA if the synchronisation failed. The
+ * word is shared by all streams and threads using the device.
+ */
+BEAM_API beam_status beam_sync_status(beam_stream_t stream);
+
+/* Short English text for a status code (static storage, never NULL). */
+BEAM_API const char* beam_status_string(beam_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+BEAM_API int beam_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Tuning and test hooks. The plain calls above use automatic choices; these
+ * variants let benchmarks and tests fix them. Same arguments and errors as the
+ * plain calls, plus `opts` (NULL = automatic).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    uint32_t flags;       /* BEAM_OPT_* bits */
+    int32_t vec_per_thread; /* 16-byte vectors per thread per row, 0 = automatic; 1..8 */
+    int32_t ctas_per_sm;  /* resident CTAs per SM for the persistent grid, 0 = automatic */
+    int32_t reserved;
+} beam_launch_opts;
+
+/* Take the exact integer row-sum path for every row instead of only for rows
+ * whose compensated sum cannot be certified (results are identical). */
+#define BEAM_OPT_FORCE_EXACT_SUM 0x1u
+
+BEAM_API beam_status beam_boundary_fused_ex(beam_stream_t stream, uint16_t* h, const uint16_t* x,
+                                   const uint16_t* post_w, const uint16_t* pre_w, int n,
+                                   float eps, int64_t T, int D, uint16_t* y_out,
+                                   const beam_launch_opts* opts);
+
+BEAM_API beam_status beam_moe_combine_boundary_ex(beam_stream_t stream, uint16_t* h,
+                                         const uint16_t* expert_out, const float* topk_w,
+                                         const uint16_t* post_w, const uint16_t* pre_w, int n,
+                                         float eps, int64_t T, int D, uint16_t* y_out,
+                                         const beam_launch_opts* opts);
+
+/*
+ * Synchronises `stream` and returns in *count the number of row sums (two per
+ * row: the post-norm and the pre-norm sum) that took the exact integer path on
+ * the current device since the last reset; reset != 0 zeroes the counter.
+ */
+BEAM_API beam_status beam_exact_sum_count(beam_stream_t stream, uint64_t* count, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEAM_BOUNDARY_H */

@@ -1,0 +1,134 @@
+"""Fused sublayer boundary of the Beam decoder on GB300 (sm_103a).
+
+Python binding of ``libbeamboundary`` (C ABI: ``include/beam_boundary.h``).
+This module only marshals torch CUDA tensors into the C calls; every step of
+the boundary runs in the library's CUDA kernels. There is no CPU or PyTorch
+fallback: without the built library, calls raise ``ImportError``.
+
+    y = boundary_fused(h, x, post_w, pre_w, n, eps)          # h updated in place
+    y = moe_combine_boundary(h, expert_out, topk_w, post_w, pre_w, n, eps)
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import LaunchOpts  # noqa: F401
+
+__all__ = ["boundary_fused", "moe_combine_boundary", "sync_status", "exact_sum_count",
+           "version", "BeamError", "LaunchOpts", "library"]
+
+
+class BeamError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.load().beam_status_string(status).decode()
+        super().__init__(f"{where}: status {status} ({msg})")
+
+
+def library() -> ctypes.CDLL:
+    """The loaded ``libbeamboundary.so`` (raises ImportError when it is not built)."""
+    return _lib.load()
+
+
+def _stream_ptr(stream) -> int | None:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream or None
+
+
+def _check(t, name: str, dtype, ndim: int):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def _opts(opts):
+    if opts is None:
+        return None
+    if isinstance(opts, dict):
+        opts = LaunchOpts(**opts)
+    return ctypes.byref(opts)
+
+
+def boundary_fused(h, x, post_w, pre_w, n: int, eps: float = 1e-6, y=None, stream=None, opts=None):
+    """Dense boundary on torch CUDA tensors; updates ``h`` in place and returns ``y``.
+
+    h, x: [T, D] bfloat16; post_w, pre_w: [D] bfloat16; n >= 1 (index of the residual add).
+    """
+    import torch
+    _check(h, "h", torch.bfloat16, 2)
+    _check(x, "x", torch.bfloat16, 2)
+    _check(post_w, "post_w", torch.bfloat16, 1)
+    _check(pre_w, "pre_w", torch.bfloat16, 1)
+    T, D = h.shape
+    if x.shape != h.shape or post_w.shape[0] != D or pre_w.shape[0] != D:
+        raise ValueError("shape mismatch: h, x [T, D]; post_w, pre_w [D]")
+    if y is None:
+        y = torch.empty_like(h)
+    _check(y, "y", torch.bfloat16, 2)
+    lib = _lib.load()
+    args = (_stream_ptr(stream), h.data_ptr(), x.data_ptr(), post_w.data_ptr(), pre_w.data_ptr(),
+            int(n), float(eps), T, D, y.data_ptr())
+    st = lib.beam_boundary_fused(*args) if opts is None else lib.beam_boundary_fused_ex(
+        *args, _opts(opts))
+    if st != 0:
+        raise BeamError(st, "beam_boundary_fused")
+    return y
+
+
+def moe_combine_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: float = 1e-6, y=None,
+                         stream=None, opts=None):
+    """MoE boundary: combine the top-8 expert outputs with FP32 weights, then the dense boundary.
+
+    h: [T, D] bf16; expert_out: [T, 8, D] bf16; topk_w: [T, 8] float32 (routing scale included).
+    """
+    import torch
+    _check(h, "h", torch.bfloat16, 2)
+    _check(expert_out, "expert_out", torch.bfloat16, 3)
+    _check(topk_w, "topk_w", torch.float32, 2)
+    _check(post_w, "post_w", torch.bfloat16, 1)
+    _check(pre_w, "pre_w", torch.bfloat16, 1)
+    T, D = h.shape
+    K = _lib.BEAM_MOE_TOPK
+    if expert_out.shape != (T, K, D) or topk_w.shape != (T, K):
+        raise ValueError(f"shape mismatch: expert_out [T, {K}, D], topk_w [T, {K}]")
+    if post_w.shape[0] != D or pre_w.shape[0] != D:
+        raise ValueError("shape mismatch: post_w, pre_w [D]")
+    if y is None:
+        y = torch.empty_like(h)
+    _check(y, "y", torch.bfloat16, 2)
+    lib = _lib.load()
+    args = (_stream_ptr(stream), h.data_ptr(), expert_out.data_ptr(), topk_w.data_ptr(),
+            post_w.data_ptr(), pre_w.data_ptr(), int(n), float(eps), T, D, y.data_ptr())
+    st = lib.beam_moe_combine_boundary(*args) if opts is None else \
+        lib.beam_moe_combine_boundary_ex(*args, _opts(opts))
+    if st != 0:
+        raise BeamError(st, "beam_moe_combine_boundary")
+    return y
+
+
+def sync_status(stream=None) -> None:
+    """Synchronise the stream and raise BeamError if a kernel reported a device-side error."""
+    st = _lib.load().beam_sync_status(_stream_ptr(stream))
+    if st != 0:
+        raise BeamError(st, "beam_sync_status")
+
+
+def exact_sum_count(reset: bool = False, stream=None) -> int:
+    """Row sums that took the exact integer path on this device (diagnostics)."""
+    v = ctypes.c_uint64(0)
+    st = _lib.load().beam_exact_sum_count(_stream_ptr(stream), ctypes.byref(v), int(reset))
+    if st != 0:
+        raise BeamError(st, "beam_exact_sum_count")
+    return int(v.value)
+
+
+def version() -> int:
+    return int(_lib.load().beam_version())

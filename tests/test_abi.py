@@ -1,0 +1,142 @@
+"""Host-only checks of the C ABI: the library builds, loads, exports every
+function ``include/beam_boundary.h`` declares, and rejects bad arguments with
+the documented status before touching CUDA (so these run without a GPU)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from sandwich_norm_residual_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "beam_boundary.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*BEAM_API\s+(?:const\s+)?\w+\s*\*?\s*(beam_\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_boundary_calls():
+    names = declared_functions()
+    for n in ("beam_boundary_fused", "beam_moe_combine_boundary", "beam_sync_status",
+              "beam_status_string", "beam_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", out, flags=re.M))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    # and nothing else of ours leaks out of the library
+    ours = {n for n in exported if n.startswith("beam")}
+    assert ours == set(declared_functions())
+    assert set(_lib.SIGNATURES) == set(declared_functions())
+
+
+def test_header_constants_match_binding():
+    text = open(HEADER).read()
+    enum = dict(re.findall(r"(BEAM_\w+)\s*=\s*(\d+)", text))
+    for name, val in enum.items():
+        assert getattr(_lib, name) == int(val), name
+    assert _lib.BEAM_MAX_D == int(re.search(r"#define BEAM_MAX_D (\d+)", text).group(1))
+    assert _lib.BEAM_MOE_TOPK == int(re.search(r"#define BEAM_MOE_TOPK (\d+)", text).group(1))
+    assert ctypes.sizeof(_lib.LaunchOpts) == 16
+
+
+def test_version_and_status_strings(lib):
+    assert lib.beam_version() == 10000
+    for s in range(0, 9):
+        assert lib.beam_status_string(s)
+    assert lib.beam_status_string(99) == b"unknown status"
+
+
+# fake device addresses: never dereferenced, the calls fail validation first
+A = 0x7F0000000000
+D = 5120
+
+
+def fused(lib, h=A, x=A + (1 << 32), pw=A + (2 << 32), qw=A + (3 << 32), n=2, eps=1e-6, T=4,
+          d=D, y=A + (4 << 32)):
+    return lib.beam_boundary_fused(None, h, x, pw, qw, n, eps, T, d, y)
+
+
+def moe(lib, h=A, e=A + (1 << 32), w=A + (5 << 32), pw=A + (2 << 32), qw=A + (3 << 32), n=2,
+        eps=1e-6, T=4, d=D, y=A + (4 << 32)):
+    return lib.beam_moe_combine_boundary(None, h, e, w, pw, qw, n, eps, T, d, y)
+
+
+@pytest.mark.parametrize("call", [fused, moe])
+def test_shape_and_argument_errors(lib, call):
+    assert call(lib, T=-1) == _lib.BEAM_ERR_SHAPE
+    assert call(lib, d=0) == _lib.BEAM_ERR_SHAPE
+    assert call(lib, d=12) == _lib.BEAM_ERR_SHAPE
+    assert call(lib, d=_lib.BEAM_MAX_D + 8) == _lib.BEAM_ERR_SHAPE
+    assert call(lib, n=0) == _lib.BEAM_ERR_ARG
+    assert call(lib, eps=-1e-6) == _lib.BEAM_ERR_ARG
+    assert call(lib, eps=float("nan")) == _lib.BEAM_ERR_ARG
+    assert call(lib, eps=float("inf")) == _lib.BEAM_ERR_ARG
+    # T = 0 is a no-op; pointers are not looked at
+    assert call(lib, T=0, h=None, y=None) == _lib.BEAM_OK
+
+
+def test_null_alignment_and_alias_errors_dense(lib):
+    assert fused(lib, h=None) == _lib.BEAM_ERR_NULL
+    assert fused(lib, x=None) == _lib.BEAM_ERR_NULL
+    assert fused(lib, pw=None) == _lib.BEAM_ERR_NULL
+    assert fused(lib, y=None) == _lib.BEAM_ERR_NULL
+    assert fused(lib, h=A + 8) == _lib.BEAM_ERR_ALIGN
+    assert fused(lib, qw=A + (3 << 32) + 2) == _lib.BEAM_ERR_ALIGN
+    assert fused(lib, y=A) == _lib.BEAM_ERR_ALIAS                 # y over h
+    assert fused(lib, y=A + (1 << 32) + 16) == _lib.BEAM_ERR_ALIAS  # y inside x
+    assert fused(lib, x=A + 3 * D * 2) == _lib.BEAM_ERR_ALIAS       # x partly over h
+    assert fused(lib, x=A + 4 * D * 2, y=A + (9 << 32)) != _lib.BEAM_ERR_ALIAS  # adjacent is fine
+    assert fused(lib, pw=A + 64) == _lib.BEAM_ERR_ALIAS             # weight inside h
+
+
+def test_null_alignment_and_alias_errors_moe(lib):
+    assert moe(lib, e=None) == _lib.BEAM_ERR_NULL
+    assert moe(lib, w=None) == _lib.BEAM_ERR_NULL
+    assert moe(lib, w=A + (5 << 32) + 4) == _lib.BEAM_ERR_ALIGN
+    assert moe(lib, y=A + (1 << 32) + 7 * D * 2 * 4) == _lib.BEAM_ERR_ALIAS  # y inside experts
+    assert moe(lib, h=A + (1 << 32) + 16) == _lib.BEAM_ERR_ALIAS            # h inside experts
+    assert moe(lib, y=A + (5 << 32)) == _lib.BEAM_ERR_ALIAS                 # y over weights
+
+
+def test_bad_launch_options_are_rejected(lib):
+    opts = _lib.LaunchOpts(flags=0x80)
+    assert lib.beam_boundary_fused_ex(None, A, A + (1 << 32), A + (2 << 32), A + (3 << 32), 2,
+                                      1e-6, 4, D, A + (4 << 32),
+                                      ctypes.byref(opts)) == _lib.BEAM_ERR_ARG
+    opts = _lib.LaunchOpts(vec_per_thread=9)
+    assert lib.beam_boundary_fused_ex(None, A, A + (1 << 32), A + (2 << 32), A + (3 << 32), 2,
+                                      1e-6, 4, D, A + (4 << 32),
+                                      ctypes.byref(opts)) == _lib.BEAM_ERR_ARG
+    # one vector per thread cannot cover D = 8192 with at most 512 threads
+    opts = _lib.LaunchOpts(vec_per_thread=1)
+    assert lib.beam_moe_combine_boundary_ex(None, A, A + (1 << 32), A + (5 << 32), A + (2 << 32),
+                                            A + (3 << 32), 2, 1e-6, 4, 8192, A + (4 << 32),
+                                            ctypes.byref(opts)) == _lib.BEAM_ERR_ARG
+
+
+def test_exact_count_rejects_null(lib):
+    assert lib.beam_exact_sum_count(None, None, 0) == _lib.BEAM_ERR_NULL
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    with pytest.raises(ImportError, match="no CPU or PyTorch fallback"):
+        _lib.load(str(tmp_path / "missing.so"))

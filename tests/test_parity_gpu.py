@@ -1,0 +1,320 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded input bytes.
+
+Gate for every output (h' and y): each BF16 element within 1 ulp of the
+oracle (ordered-integer distance) and >= 99.99% bit-identical. The kernels'
+row sums are exact (certified compensated sum, exact integer fallback), so
+these tests expect and report 100%.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sandwich_norm_residual_gb300 as snr
+import synth
+from parity import assert_parity, bits
+from sandwich_norm_residual_gb300 import build
+from synth import CONFIGS
+
+pytestmark = pytest.mark.gpu
+THREADS = max(1, min(32, os.cpu_count() or 1))
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build.build()
+    snr.library()
+    torch.cuda.init()
+
+
+def to_dev(inp: dict) -> dict:
+    return {k: v.to(DEV) for k, v in inp.items()}
+
+
+def gpu_dense(inp, n, eps, opts=None, stream=None):
+    d = to_dev(inp)
+    y = snr.boundary_fused(d["h"], d["x"], d["post_w"], d["pre_w"], n, eps, opts=opts,
+                           stream=stream)
+    snr.sync_status(stream)
+    return bits(d["h"]), bits(y)
+
+
+def gpu_moe(inp, n, eps, opts=None):
+    d = to_dev(inp)
+    y = snr.moe_combine_boundary(d["h"], d["expert_out"], d["topk_w"], d["post_w"], d["pre_w"],
+                                 n, eps, opts=opts)
+    snr.sync_status()
+    return bits(d["h"]), bits(y)
+
+
+def oracle_dense(inp, n, eps):
+    return oracle.boundary(inp["h"], inp["x"], inp["post_w"], inp["pre_w"], n, eps,
+                           threads=THREADS)
+
+
+def oracle_moe(inp, n, eps):
+    return oracle.moe_boundary(inp["h"], inp["expert_out"], inp["topk_w"], inp["post_w"],
+                               inp["pre_w"], n, eps, threads=THREADS)
+
+
+def check(got, want, label):
+    st_h = assert_parity(got[0], want[0], f"{label} h'")
+    st_y = assert_parity(got[1], want[1], f"{label} y")
+    print(f"{label}: h' {st_h}  y {st_y}")
+    return st_h, st_y
+
+
+def bf16(a) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def random_dense(T, D, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return dict(h=bf16(rng.standard_normal((T, D))), x=bf16(rng.standard_normal((T, D)) * scale),
+                post_w=bf16(1 + 0.1 * rng.standard_normal(D)),
+                pre_w=bf16(1 + 0.1 * rng.standard_normal(D)))
+
+
+# --------------------------------------------------------------- the five workloads
+
+def test_config0_dense_decode():
+    cfg = CONFIGS[0]
+    inp = synth.dense_inputs(cfg)
+    check(gpu_dense(inp, cfg.n, cfg.eps), oracle_dense(inp, cfg.n, cfg.eps), cfg.name)
+
+
+def test_config1_decode_chain_every_step_and_unit_variance():
+    cfg = CONFIGS[1]
+    h0 = synth.dense_inputs(cfg)["h"]
+    h_gpu = h0.to(DEV)
+    h_ref = oracle.as_u16(h0).copy()
+    xn_sq = 0.0
+    for s in range(cfg.steps):
+        n = cfg.n + s
+        inp = synth.dense_inputs(cfg, step=s)
+        d = to_dev(inp)
+        y = snr.boundary_fused(h_gpu, d["x"], d["post_w"], d["pre_w"], n, cfg.eps)
+        h_ref, y_ref = oracle.boundary(h_ref, inp["x"], inp["post_w"], inp["pre_w"], n, cfg.eps,
+                                       threads=THREADS)
+        snr.sync_status()
+        assert_parity(bits(h_gpu), h_ref, f"chain step {s} h'")
+        assert_parity(bits(y), y_ref, f"chain step {s} y")
+        xn = np.stack([oracle.rmsnorm(inp["x"][t], inp["post_w"], cfg.eps) for t in range(cfg.T)])
+        xnf = (xn.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        xn_sq += float(np.mean(xnf * xnf))
+    # depth scaling keeps the stream at (var(h_1) + sum_n mean(xn_n^2)) / N
+    h1 = h0.float().numpy().astype(np.float64)
+    pred = (np.mean(h1 * h1) + xn_sq) / (cfg.steps + 1)
+    got = float(np.mean(h_gpu.float().cpu().numpy().astype(np.float64) ** 2))
+    sigma = np.sqrt(2.0 / h1.size)
+    assert abs(got - pred) < 5 * sigma, (got, pred)
+
+
+def test_config2_dense_prefill_full():
+    cfg = CONFIGS[2]
+    inp = synth.dense_inputs(cfg)
+    check(gpu_dense(inp, cfg.n, cfg.eps), oracle_dense(inp, cfg.n, cfg.eps), cfg.name)
+
+
+def test_config3_moe_full():
+    cfg = CONFIGS[3]
+    inp = synth.moe_inputs(cfg)
+    check(gpu_moe(inp, cfg.n, cfg.eps), oracle_moe(inp, cfg.n, cfg.eps), cfg.name)
+
+
+@pytest.mark.slow
+def test_config4_moe_stress_full_size_sampled_rows():
+    """T = 131072 on the GPU in one launch; the oracle checks 1024 sampled rows,
+    half of them tokens with a x100 outlier expert row."""
+    cfg = CONFIGS[4]
+    T, D, K = cfg.T, cfg.D, cfg.K
+    e = torch.empty((T, K, D), dtype=torch.bfloat16, device=DEV)
+    chunk = 2048
+    for r in range(0, T, chunk):
+        m = min(chunk, T - r)
+        e[r:r + m].copy_(synth.expert_rows(cfg, r, m))
+    h = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["h"], T * D).reshape(T, D)).to(DEV)
+    w = torch.from_numpy(synth.topk_weights(cfg.seed, synth.STREAMS["topk"], T, K,
+                                            cfg.route_scale)).to(DEV)
+    pw = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["post_w"], D, 0, 0.1, 1.0))
+    qw = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["pre_w"], D, 0, 0.1, 1.0))
+    h_in = h.clone()
+    y = snr.moe_combine_boundary(h, e, w, pw.to(DEV), qw.to(DEV), cfg.n, cfg.eps)
+    snr.sync_status()
+    outl = synth.bernoulli(cfg.seed, synth.STREAMS["outlier"], T * K, cfg.outlier_p)
+    outl_tok = np.unique(np.nonzero(outl)[0] // K)
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([rng.choice(outl_tok, min(512, outl_tok.size), replace=False),
+                                     rng.choice(T, 512, replace=False)]))
+    idx = torch.from_numpy(rows).to(DEV)
+    inp = dict(h=h_in[idx].cpu(), expert_out=e[idx].cpu(), topk_w=w[idx].cpu(), post_w=pw,
+               pre_w=qw)
+    want = oracle_moe(inp, cfg.n, cfg.eps)
+    check((bits(h[idx]), bits(y[idx])), want, f"{cfg.name} ({rows.size} sampled rows)")
+    # sampled rows must equal a fresh generation of the same rows (the bytes the oracle saw)
+    r0 = int(rows[0])
+    assert torch.equal(inp["expert_out"][0], synth.expert_rows(cfg, r0, 1)[0])
+
+
+# --------------------------------------------------------------- shapes and edge cases
+
+@pytest.mark.parametrize("T,D,n", [(1, 5120, 2), (3, 5120, 104), (7, 5120, 105), (1000, 5120, 7),
+                                   (5, 8, 2), (9, 128, 3), (33, 8192, 20), (2, 16, 1),
+                                   (300, 4096, 52), (4, 32768, 9), (17, 1000, 5)])
+def test_dense_shapes(T, D, n):
+    inp = random_dense(T, D, seed=T * 7 + D)
+    check(gpu_dense(inp, n, 1e-6), oracle_dense(inp, n, 1e-6), f"dense T={T} D={D} n={n}")
+
+
+@pytest.mark.parametrize("T,D,n", [(1, 5120, 20), (3, 5120, 2), (257, 5120, 104), (6, 8, 3),
+                                   (11, 2048, 1), (2, 32768, 50), (13, 1000, 4)])
+def test_moe_shapes(T, D, n):
+    rng = np.random.default_rng(T + D)
+    z = rng.standard_normal((T, 8))
+    s = 1 / (1 + np.exp(-z))
+    inp = dict(h=bf16(rng.standard_normal((T, D))),
+               expert_out=bf16(rng.standard_normal((T, 8, D))),
+               topk_w=torch.from_numpy((2.5 * s / s.sum(1, keepdims=True)).astype(np.float32)),
+               post_w=bf16(1 + 0.1 * rng.standard_normal(D)),
+               pre_w=bf16(1 + 0.1 * rng.standard_normal(D)))
+    check(gpu_moe(inp, n, 1e-6), oracle_moe(inp, n, 1e-6), f"moe T={T} D={D} n={n}")
+
+
+def test_zero_rows_eps_zero_and_outlier_rows():
+    T, D = 12, 5120
+    inp = random_dense(T, D, seed=5)
+    x = inp["x"].float()
+    x[0] = 0.0                      # zero branch: r1 = 1/sqrt(eps)
+    x[1] *= 100.0                   # outlier row
+    x[2] *= 1e-25                   # tiny: squares underflow or turn subnormal
+    x[3, ::7] *= 3e4                # a few huge elements
+    x[4] = 1e19                     # squares near the FP32 range; the sum overflows
+    inp["x"] = x.to(torch.bfloat16)
+    h = inp["h"].float()
+    h[5] = 0.0
+    inp["h"] = h.to(torch.bfloat16)
+    for eps in (1e-6, 0.0):
+        if eps == 0.0:
+            inp["x"][0] = inp["x"][6]  # eps = 0 only on rows that are not all zero
+            inp["h"][5] = inp["h"][7]
+        check(gpu_dense(inp, 3, eps), oracle_dense(inp, 3, eps), f"edge rows eps={eps}")
+
+
+def test_non_finite_inputs_propagate_like_the_oracle():
+    T, D = 4, 512
+    inp = random_dense(T, D, seed=6)
+    inp["x"][0, 5] = float("inf")
+    inp["x"][1, 9] = float("nan")
+    inp["h"][2, 3] = float("-inf")
+    check(gpu_dense(inp, 2, 1e-6), oracle_dense(inp, 2, 1e-6), "non-finite")
+
+
+def test_rows_at_rounding_ties_take_the_exact_path():
+    """Rows whose exact sum of squares sits on (or within 2^-40 of) an FP32
+    midpoint cannot be certified; the exact path must decide, bit for bit."""
+    T, D = 8, 5120
+    rng = np.random.default_rng(8)
+    x = np.zeros((T, D), np.float32)
+    for t in range(T):
+        x[t, 0] = 1.0
+        x[t, 1] = 2.0 ** -12            # square 2^-24: 1 + 2^-24 is an FP32 tie
+        if t % 2:
+            x[t, 2] = 2.0 ** -20        # square 2^-40 breaks the tie upwards
+        x[t, 3:3 + 64] = rng.choice([2.0 ** -30, 0.0], 64).astype(np.float32)
+    inp = dict(h=bf16(rng.standard_normal((T, D))), x=bf16(x),
+               post_w=bf16(np.ones(D)), pre_w=bf16(np.ones(D)))
+    snr.exact_sum_count(reset=True)
+    check(gpu_dense(inp, 2, 0.0), oracle_dense(inp, 2, 0.0), "tie rows")
+    assert snr.exact_sum_count() >= T
+
+
+def test_launch_shape_does_not_change_a_bit():
+    T, D = 200, 5120
+    inp = random_dense(T, D, seed=10)
+    ref = None
+    for vpt in (2, 3, 4, 5, 6, 7, 8):  # one vector per thread would need 640 threads
+        for per_sm in (0, 1):
+            got = gpu_dense(inp, 11, 1e-6, opts=dict(vec_per_thread=vpt, ctas_per_sm=per_sm))
+            if ref is None:
+                ref = got
+                check(got, oracle_dense(inp, 11, 1e-6), "vpt sweep reference")
+            assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), (vpt, per_sm)
+
+
+def test_forced_exact_path_is_bit_identical_and_counted():
+    T, D = 300, 5120
+    inp = random_dense(T, D, seed=12)
+    fast = gpu_dense(inp, 4, 1e-6)
+    snr.exact_sum_count(reset=True)
+    exact = gpu_dense(inp, 4, 1e-6, opts=dict(flags=snr._lib.BEAM_OPT_FORCE_EXACT_SUM))
+    assert snr.exact_sum_count() == 2 * T
+    assert np.array_equal(fast[0], exact[0]) and np.array_equal(fast[1], exact[1])
+    cfg = CONFIGS[3]
+    m = synth.moe_inputs(cfg, rows=64)
+    a = gpu_moe(m, cfg.n, cfg.eps)
+    b = gpu_moe(m, cfg.n, cfg.eps, opts=dict(flags=snr._lib.BEAM_OPT_FORCE_EXACT_SUM))
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    check(b, oracle_moe(m, cfg.n, cfg.eps), "moe forced exact")
+
+
+def test_certification_is_rare_on_the_prefill_workload():
+    cfg = CONFIGS[2]
+    inp = synth.dense_inputs(cfg)
+    snr.exact_sum_count(reset=True)
+    gpu_dense(inp, cfg.n, cfg.eps)
+    n_exact = snr.exact_sum_count()
+    print(f"exact-path row sums: {n_exact} of {2 * cfg.T}")
+    assert n_exact <= 2 * cfg.T * 1e-3
+
+
+def test_branch_may_be_the_stream_itself():
+    T, D = 16, 5120
+    inp = random_dense(T, D, seed=13)
+    d = to_dev(inp)
+    y = snr.boundary_fused(d["h"], d["h"], d["post_w"], d["pre_w"], 6, 1e-6)
+    snr.sync_status()
+    want = oracle.boundary(inp["h"], inp["h"], inp["post_w"], inp["pre_w"], 6, 1e-6)
+    check((bits(d["h"]), bits(y)), want, "x is h")
+
+
+def test_guard_bands_and_untouched_neighbours():
+    """Operands sit inside larger buffers filled with a canary; nothing outside
+    the operands may change (a bounds check without compute-sanitizer)."""
+    T, D, pad = 37, 5120, 4096
+    inp = random_dense(T, D, seed=14)
+    canary = torch.tensor(0x7E5A, dtype=torch.int16)
+
+    def padded(t):
+        flat = torch.full((t.numel() + 2 * pad,), 0x7E5A, dtype=torch.int16, device=DEV)
+        flat[pad:pad + t.numel()].copy_(t.reshape(-1).view(torch.int16))
+        return flat
+
+    bufs = {k: padded(v) for k, v in inp.items()}
+    ybuf = torch.full((T * D + 2 * pad,), 0x7E5A, dtype=torch.int16, device=DEV)
+    view = {k: b[pad:pad + inp[k].numel()].view(torch.bfloat16).reshape(inp[k].shape)
+            for k, b in bufs.items()}
+    y = ybuf[pad:pad + T * D].view(torch.bfloat16).reshape(T, D)
+    snr.boundary_fused(view["h"], view["x"], view["post_w"], view["pre_w"], 2, 1e-6, y=y)
+    snr.sync_status()
+    for b in list(bufs.values()) + [ybuf]:
+        assert (b[:pad] == canary).all() and (b[-pad:] == canary).all()
+    assert torch.equal(bufs["x"][pad:-pad].cpu(), inp["x"].reshape(-1).view(torch.int16))
+    check((bits(view["h"]), bits(y)), oracle_dense(inp, 2, 1e-6), "guard bands")
+
+
+def test_zero_tokens_is_a_no_op_and_streams_are_honoured():
+    h = torch.zeros((0, 5120), dtype=torch.bfloat16, device=DEV)
+    w = torch.ones(5120, dtype=torch.bfloat16, device=DEV)
+    y = snr.boundary_fused(h, h, w, w, 2, 1e-6)
+    assert y.shape == (0, 5120)
+    inp = random_dense(64, 5120, seed=15)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        got = gpu_dense(inp, 9, 1e-6, stream=s)
+    check(got, oracle_dense(inp, 9, 1e-6), "side stream")
