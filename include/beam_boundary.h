@@ -144,15 +144,27 @@ BEAM_API int beam_version(void);
  * plain calls, plus `opts` (NULL = automatic).
  * ------------------------------------------------------------------------ */
 typedef struct {
-    uint32_t flags;       /* BEAM_OPT_* bits */
+    uint32_t flags;         /* BEAM_OPT_* bits */
     int32_t vec_per_thread; /* 16-byte vectors per thread per row, 0 = automatic; 1..8 */
-    int32_t ctas_per_sm;  /* resident CTAs per SM for the persistent grid, 0 = automatic */
-    int32_t reserved;
+    int32_t ctas_per_sm;    /* resident CTAs per SM for the persistent grid, 0 = automatic */
+    int32_t prefetch_rows;  /* kernels loading straight to registers: rows ahead (per CTA)
+                               whose inputs are bulk-prefetched into L2;
+                               0 = automatic, -1 = none, 1..8 */
+    int32_t stages;         /* dense boundary: shared-memory ring slots per CTA fed by bulk
+                               copies, 2..8; -1 = no ring (loads straight to registers);
+                               0 = automatic (no ring, which measured faster at D = 5120,
+                               unless BEAM_OPT_TEST_WAIT_TIMEOUT asks for the ring) */
+    int32_t reserved[3];    /* must be 0 */
 } beam_launch_opts;
 
 /* Take the exact integer row-sum path for every row instead of only for rows
  * whose compensated sum cannot be certified (results are identical). */
 #define BEAM_OPT_FORCE_EXACT_SUM 0x1u
+/* Test hook for the bounded waits (dense boundary, ring kernel only): every CTA
+ * first waits on an mbarrier that nothing completes; the wait gives up after
+ * 1 ms, the device status word records it (beam_sync_status then returns
+ * BEAM_ERR_TIMEOUT) and the launch carries on normally. */
+#define BEAM_OPT_TEST_WAIT_TIMEOUT 0x2u
 
 BEAM_API beam_status beam_boundary_fused_ex(beam_stream_t stream, uint16_t* h, const uint16_t* x,
                                    const uint16_t* post_w, const uint16_t* pre_w, int n,

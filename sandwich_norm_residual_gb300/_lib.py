@@ -20,12 +20,15 @@ BEAM_ERR_DEVICE = 8
 BEAM_MAX_D = 32768
 BEAM_MOE_TOPK = 8
 BEAM_OPT_FORCE_EXACT_SUM = 0x1
+BEAM_OPT_TEST_WAIT_TIMEOUT = 0x2
 
 
 class LaunchOpts(ctypes.Structure):
-    """``beam_launch_opts``: flags, vectors per thread, CTAs per SM (0 = automatic)."""
+    """``beam_launch_opts``: flags, vectors per thread, CTAs per SM, L2 prefetch distance,
+    ring stages (0 = automatic for each)."""
     _fields_ = [("flags", ctypes.c_uint32), ("vec_per_thread", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("prefetch_rows", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 # name -> (restype, argtypes)

@@ -21,32 +21,74 @@ using KernelFn = void (*)(BoundaryParams);
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxVpt = 8;
+constexpr int kMaxPrefetch = 8;
+constexpr int kAutoPrefetch = 1;       // rows ahead prefetched into L2 (register kernels)
+constexpr int kAutoStages = -1;        // dense: registers + L2 prefetch measured faster than the ring
+constexpr int kTestStages = 2;         // ring slots when only the wait test hook asks for the ring
+constexpr uint64_t kWaitNs = 2000000000ull;    // every mbarrier wait gives up after 2 s
+constexpr uint64_t kTestWaitNs = 1000000ull;   // the test hook's wait: 1 ms
 
-__device__ unsigned int g_status_word;  // device-side error word (bounded waits)
+enum KernelKind { kDenseRegs = 0, kMoeRegs = 1, kDenseRing = 2 };
+
+struct OccKey {
+    KernelFn fn;
+    int nt, smem;
+};
 
 struct DeviceInfo {
     bool checked = false;
     bool ok = false;
     int sms = 0;
-    int occ[2][kMaxVpt + 1][beam::kMaxThreads / 32 + 1] = {};  // resident CTAs per SM, 0 = unknown
+    int smem_optin = 0;                       // max dynamic + static shared memory per CTA
+    KernelFn lim_fn[64] = {};                 // kernels whose dynamic smem limit was raised
+    int lim_val[64] = {};
+    int lim_n = 0;
+    OccKey occ_key[128] = {};
+    int occ_val[128] = {};
+    int occ_n = 0;
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
-template <bool MOE>
-KernelFn kernel_for(int vpt) {
+// FULL kernels (row = exactly NT * VPT vectors, weights staged in shared
+// memory) exist for these vectors-per-thread values
+bool has_full(int vpt) { return vpt >= 2 && vpt <= 5; }
+
+template <int V, int KIND, bool FULL>
+KernelFn pick() {
+    if (KIND == kDenseRing) return beam::boundary_ring_kernel<V, FULL>;
+    return beam::boundary_kernel<V, KIND == kMoeRegs, FULL>;
+}
+
+template <int KIND>
+KernelFn kernel_for(int vpt, bool full) {
+    if (full) {
+        switch (vpt) {
+        case 2: return pick<2, KIND, true>();
+        case 3: return pick<3, KIND, true>();
+        case 4: return pick<4, KIND, true>();
+        case 5: return pick<5, KIND, true>();
+        default: return nullptr;
+        }
+    }
     switch (vpt) {
-    case 1: return beam::boundary_kernel<1, MOE>;
-    case 2: return beam::boundary_kernel<2, MOE>;
-    case 3: return beam::boundary_kernel<3, MOE>;
-    case 4: return beam::boundary_kernel<4, MOE>;
-    case 5: return beam::boundary_kernel<5, MOE>;
-    case 6: return beam::boundary_kernel<6, MOE>;
-    case 7: return beam::boundary_kernel<7, MOE>;
-    case 8: return beam::boundary_kernel<8, MOE>;
+    case 1: return pick<1, KIND, false>();
+    case 2: return pick<2, KIND, false>();
+    case 3: return pick<3, KIND, false>();
+    case 4: return pick<4, KIND, false>();
+    case 5: return pick<5, KIND, false>();
+    case 6: return pick<6, KIND, false>();
+    case 7: return pick<7, KIND, false>();
+    case 8: return pick<8, KIND, false>();
     default: return nullptr;
     }
+}
+
+KernelFn kernel_for_kind(int kind, int vpt, bool full) {
+    return kind == kDenseRing ? kernel_for<kDenseRing>(vpt, full)
+           : kind == kMoeRegs ? kernel_for<kMoeRegs>(vpt, full)
+                              : kernel_for<kDenseRegs>(vpt, full);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -64,11 +106,12 @@ int threads_for(int nvec, int vpt) {
     return nt <= beam::kMaxThreads ? nt : 0;
 }
 
-// Automatic vectors per thread: the first candidate whose CTA wastes under
-// 1/16 of its slots, else the smallest that fits.
+// Automatic vectors per thread: the first preferred value whose CTA wastes
+// under 1/16 of its slots, else the smallest that fits. The preferences come
+// from sweeps at D = 5120 on GB300 (dense: 5 -> 128 threads; MoE: 2 -> 320).
 int choose_vpt(int nvec, bool moe) {
-    static const int dense_pref[] = {4, 2, 5, 3, 6, 8, 1, 7};
-    static const int moe_pref[] = {2, 1, 3, 4, 5, 6, 8, 7};
+    static const int dense_pref[] = {5, 4, 6, 3, 2, 8, 7, 1};
+    static const int moe_pref[] = {2, 3, 4, 1, 5, 6, 8, 7};
     const int* pref = moe ? moe_pref : dense_pref;
     for (int i = 0; i < 8; ++i) {
         int v = pref[i], nt = threads_for(nvec, v);
@@ -97,7 +140,7 @@ float error_factor(int vpt, int nt) {
     return (float)(E * u * u * 1.5 * (1.0 + 1.0 / 1024.0));
 }
 
-beam_status current_device(int* dev_out, DeviceInfo** info) {
+beam_status current_device(DeviceInfo** info) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -107,36 +150,75 @@ beam_status current_device(int* dev_out, DeviceInfo** info) {
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceInfo& d = g_dev[dev];
     if (!d.checked) {
-        int major = 0, minor = 0, sms = 0;
+        int major = 0, minor = 0, sms = 0, optin = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
             cudaGetLastError();
             return BEAM_ERR_CUDA;
         }
         d.ok = (major == 10 && minor == 3);
         d.sms = sms;
+        d.smem_optin = optin;
         d.checked = true;
     }
     if (!d.ok) return BEAM_ERR_DEVICE;
-    *dev_out = dev;
     *info = &d;
     return BEAM_OK;
 }
 
-beam_status resident_ctas(DeviceInfo* d, bool moe, int vpt, int nt, KernelFn fn, int* out) {
+// Dynamic shared memory `fn` may use (the opt-in maximum less its static
+// shared memory); raises the kernel's limit to it on first use.
+beam_status smem_limit(DeviceInfo* d, KernelFn fn, int* out) {
     std::lock_guard<std::mutex> lk(g_mu);
-    int& slot = d->occ[moe ? 1 : 0][vpt][nt / 32];
-    if (slot == 0) {
-        int nb = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, reinterpret_cast<const void*>(fn), nt, 0) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return BEAM_ERR_CUDA;
+    for (int i = 0; i < d->lim_n; ++i)
+        if (d->lim_fn[i] == fn) {
+            *out = d->lim_val[i];
+            return BEAM_OK;
         }
-        slot = nb > 0 ? nb : 1;
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void*>(fn)) != cudaSuccess) {
+        cudaGetLastError();
+        return BEAM_ERR_CUDA;
     }
-    *out = slot;
+    int limit = d->smem_optin - (int)attr.sharedSizeBytes;
+    if (limit < 0) limit = 0;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             limit) != cudaSuccess) {
+        cudaGetLastError();
+        return BEAM_ERR_CUDA;
+    }
+    if (d->lim_n < 64) {
+        d->lim_fn[d->lim_n] = fn;
+        d->lim_val[d->lim_n++] = limit;
+    }
+    *out = limit;
+    return BEAM_OK;
+}
+
+// resident CTAs per SM of `fn` with `nt` threads and `smem` dynamic bytes (cached)
+beam_status resident_ctas(DeviceInfo* d, KernelFn fn, int nt, int smem, int* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < d->occ_n; ++i) {
+        const OccKey& k = d->occ_key[i];
+        if (k.fn == fn && k.nt == nt && k.smem == smem) {
+            *out = d->occ_val[i];
+            return BEAM_OK;
+        }
+    }
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, reinterpret_cast<const void*>(fn), nt, smem) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return BEAM_ERR_CUDA;
+    }
+    nb = nb > 0 ? nb : 1;
+    if (d->occ_n < 128) {
+        d->occ_key[d->occ_n] = OccKey{fn, nt, smem};
+        d->occ_val[d->occ_n++] = nb;
+    }
+    *out = nb;
     return BEAM_OK;
 }
 
@@ -145,8 +227,11 @@ beam_status check_common(int n, float eps, int64_t T, int D, const beam_launch_o
     if (n < 1 || !(eps >= 0.0f) || !std::isfinite(eps)) return BEAM_ERR_ARG;
     if (opts) {
         if (opts->vec_per_thread < 0 || opts->vec_per_thread > kMaxVpt || opts->ctas_per_sm < 0 ||
-            (opts->flags & ~BEAM_OPT_FORCE_EXACT_SUM))
+            opts->prefetch_rows < -1 || opts->prefetch_rows > kMaxPrefetch || opts->stages < -1 ||
+            opts->stages == 1 || opts->stages > beam::kMaxStages || opts->reserved[0] || opts->reserved[1] ||
+            opts->reserved[2] || (opts->flags & ~(BEAM_OPT_FORCE_EXACT_SUM | BEAM_OPT_TEST_WAIT_TIMEOUT)))
             return BEAM_ERR_ARG;
+        if ((opts->flags & BEAM_OPT_TEST_WAIT_TIMEOUT) && opts->stages == -1) return BEAM_ERR_ARG;
         if (opts->vec_per_thread && !threads_for(D / 8, opts->vec_per_thread)) return BEAM_ERR_ARG;
     }
     return BEAM_OK;
@@ -155,19 +240,63 @@ beam_status check_common(int n, float eps, int64_t T, int D, const beam_launch_o
 beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* x, const uint16_t* e,
                    const float* w, const uint16_t* post_w, const uint16_t* pre_w, int n, float eps,
                    int64_t T, int D, uint16_t* y, const beam_launch_opts* opts) {
-    int dev = 0;
     DeviceInfo* info = nullptr;
-    beam_status st = current_device(&dev, &info);
+    beam_status st = current_device(&info);
     if (st != BEAM_OK) return st;
 
     const int nvec = D / 8;
     const int vpt = (opts && opts->vec_per_thread) ? opts->vec_per_thread : choose_vpt(nvec, moe);
     const int nt = threads_for(nvec, vpt);
-    KernelFn fn = moe ? kernel_for<true>(vpt) : kernel_for<false>(vpt);
-    if (!fn || !nt) return BEAM_ERR_SHAPE;
+    if (!nt) return BEAM_ERR_SHAPE;
+
+    // FULL: the row is exactly nt * vpt vectors; its kernels stage the FP32
+    // weights (8 D bytes) in shared memory
+    const bool full = has_full(vpt) && nt * vpt == nvec;
+    const int wbytes = full ? 8 * D : 0;
+    const int slot_bytes = 4 * D;
+    int kind = moe ? kMoeRegs : kDenseRing;
+    int stages = 0;
+    KernelFn fn = nullptr;
+    int limit = 0;
+    if (!moe) {
+        // dense rows go through the shared-memory ring when at least two slots fit
+        int want = (opts && opts->stages) ? opts->stages : kAutoStages;
+        if (want == -1 && opts && !opts->stages && (opts->flags & BEAM_OPT_TEST_WAIT_TIMEOUT)) want = kTestStages;
+        if (want == -1) {
+            kind = kDenseRegs;
+        } else {
+            fn = kernel_for_kind(kDenseRing, vpt, full);
+            if (!fn) return BEAM_ERR_SHAPE;
+            st = smem_limit(info, fn, &limit);
+            if (st != BEAM_OK) return st;
+            const int max_slots = (limit - wbytes) / slot_bytes;
+            if (want <= max_slots) {
+                stages = want;
+            } else if (opts && opts->stages > 0) {
+                return BEAM_ERR_ARG;  // asked for more slots than fit
+            } else if (max_slots >= 2) {
+                stages = max_slots < beam::kMaxStages ? max_slots : beam::kMaxStages;
+            } else {
+                if (opts && (opts->flags & BEAM_OPT_TEST_WAIT_TIMEOUT)) return BEAM_ERR_ARG;
+                kind = kDenseRegs;
+            }
+        }
+    }
+    if (kind != kDenseRing) {
+        fn = kernel_for_kind(kind, vpt, full);
+        if (!fn) return BEAM_ERR_SHAPE;
+        st = smem_limit(info, fn, &limit);
+        if (st != BEAM_OK) return st;
+        if (wbytes > limit) {  // weights do not fit: the generic kernel reads them from global memory
+            fn = kernel_for_kind(kind, vpt, false);
+            if (!fn) return BEAM_ERR_SHAPE;
+        }
+    }
+    const bool full_used = (kind == kDenseRing) ? full : (full && wbytes <= limit);
+    const int smem = (kind == kDenseRing ? stages * slot_bytes : 0) + (full_used ? wbytes : 0);
 
     int per_sm = 0;
-    st = resident_ctas(info, moe, vpt, nt, fn, &per_sm);
+    st = resident_ctas(info, fn, nt, smem, &per_sm);
     if (st != BEAM_OK) return st;
     if (opts && opts->ctas_per_sm) per_sm = opts->ctas_per_sm < per_sm ? opts->ctas_per_sm : per_sm;
     int64_t grid = (int64_t)per_sm * info->sms;
@@ -188,11 +317,18 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
     p.c2 = (float)(1.0 / std::sqrt((double)n));
     p.eps = eps;
     p.errk = error_factor(vpt, nt);
-    p.flags = (opts && (opts->flags & BEAM_OPT_FORCE_EXACT_SUM)) ? beam::kFlagForceExact : 0u;
+    p.flags = 0u;
+    if (opts && (opts->flags & BEAM_OPT_FORCE_EXACT_SUM)) p.flags |= beam::kFlagForceExact;
+    if (opts && (opts->flags & BEAM_OPT_TEST_WAIT_TIMEOUT)) p.flags |= beam::kFlagTestWaitTimeout;
+    p.prefetch_rows = (opts && opts->prefetch_rows) ? (opts->prefetch_rows < 0 ? 0 : opts->prefetch_rows)
+                                                    : kAutoPrefetch;
+    p.stages = stages;
+    p.wait_ns = kWaitNs;
+    p.test_wait_ns = kTestWaitNs;
 
     void* args[] = {&p};
     cudaError_t err = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3((unsigned)grid), dim3(nt), args,
-                                       0, reinterpret_cast<cudaStream_t>(stream));
+                                       (size_t)smem, reinterpret_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) {
         cudaGetLastError();
         return BEAM_ERR_CUDA;
@@ -262,8 +398,8 @@ beam_status beam_sync_status(beam_stream_t stream) {
         return BEAM_ERR_CUDA;
     }
     unsigned int word = 0, zero = 0;
-    if (cudaMemcpyFromSymbolAsync(&word, g_status_word, sizeof word, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyToSymbolAsync(g_status_word, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+    if (cudaMemcpyFromSymbolAsync(&word, beam::g_status_word, sizeof word, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(beam::g_status_word, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return BEAM_ERR_CUDA;

@@ -19,6 +19,7 @@
 #pragma once
 
 #include "row_sum.cuh"
+#include "tma.cuh"
 
 namespace beam {
 
@@ -36,9 +37,15 @@ struct BoundaryParams {
     float c1, c2, eps;
     float errk;             // certified-rounding error factor for this launch shape
     unsigned flags;
+    int prefetch_rows;      // rows of this CTA's sequence to prefetch into L2 ahead of use
+    int stages;             // ring slots per CTA (ring kernel)
+    unsigned long long wait_ns;       // bound of every mbarrier wait
+    unsigned long long test_wait_ns;  // bound of the test hook's wait
 };
 
 constexpr unsigned kFlagForceExact = 1u;
+constexpr unsigned kFlagTestWaitTimeout = 2u;
+constexpr int kMaxStages = 8;
 constexpr int kMaxThreads = 512;
 constexpr int kTopK = 8;
 
@@ -65,6 +72,21 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16)
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
+// One thread asks L2 for the inputs of row r (branch rows and h)
+template <bool MOE>
+__device__ __forceinline__ void prefetch_row(const BoundaryParams& p, long long r) {
+    if (r >= p.T) return;
+    const uint32_t row_bytes = (uint32_t)p.D * 2u;
+    if (MOE) prefetch_l2(p.e + (size_t)r * kTopK * (size_t)p.D, row_bytes * kTopK);
+    else prefetch_l2(p.x + (size_t)r * (size_t)p.D, row_bytes);
+    prefetch_l2(p.h + (size_t)r * (size_t)p.D, row_bytes);
+}
+
 __device__ __forceinline__ uint32_t word(const uint4& v, int q) {
     return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
@@ -72,14 +94,23 @@ __device__ __forceinline__ void set_word(uint4& v, int q, uint32_t w) {
     if (q == 0) v.x = w; else if (q == 1) v.y = w; else if (q == 2) v.z = w; else v.w = w;
 }
 
+// Shared memory of the block reduction: one (sum, compensation) pair per
+// thread, and the certified result broadcast by warp 0.
+struct RedScratch {
+    float2 part[kMaxThreads];
+    float2 result;  // (rounded sum, 1 if certified else 0)
+};
+
 // Block-wide compensated sum of the squares of the row held in v[] (zeros in
-// unused slots). Returns true with *out = RN32(exact sum) when the rounding
-// is certified; false when the exact path must decide. The barrier inside
-// also orders every store this block issued before the call ahead of any
-// load after it (the exact path re-reads rows through L2).
+// unused slots). Every thread folds its two FP32 lanes into one pair and
+// stores it; warp 0 merges the pairs (lane l takes l, l+32, ... in order, then
+// a 5-level xor butterfly), certifies the rounding and broadcasts it. Returns
+// true with *out = RN32(exact sum) when certified; false when the exact path
+// must decide. The first barrier also orders every store this block issued
+// before the call ahead of any load after it (the exact path re-reads rows).
 template <int VPT>
-__device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float errk,
-                                                  float2 (*red)[32], int& buf, float* out) {
+__device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float errk, RedScratch* rs,
+                                                  float* out) {
     float2 s = make_float2(0.f, 0.f), c = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
@@ -90,24 +121,44 @@ __device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float e
         }
     float S = s.x, C = c.x;
     ff_merge(S, C, s.y, c.y);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-        float s2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
-        float c2 = __shfl_xor_sync(0xFFFFFFFFu, C, off);
-        ff_merge(S, C, s2, c2);
-    }
-    const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    if ((threadIdx.x & 31) == 0) red[buf][warp] = make_float2(S, C);
+    rs->part[threadIdx.x] = make_float2(S, C);
     __syncthreads();
-    float2 t0 = red[buf][0];
-    S = t0.x;
-    C = t0.y;
-    for (int w = 1; w < nw; ++w) {
-        float2 tw = red[buf][w];
-        ff_merge(S, C, tw.x, tw.y);
+    if (threadIdx.x < 32) {
+        const int nw = blockDim.x >> 5;
+        float2 t0 = rs->part[threadIdx.x];
+        S = t0.x;
+        C = t0.y;
+        for (int w = 1; w < nw; ++w) {
+            float2 tw = rs->part[threadIdx.x + 32 * w];
+            ff_merge(S, C, tw.x, tw.y);
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            float s2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
+            float c2 = __shfl_xor_sync(0xFFFFFFFFu, C, off);
+            ff_merge(S, C, s2, c2);
+        }
+        if (threadIdx.x == 0) {
+            float r;
+            bool ok = certify_round(S, C, errk, &r);
+            rs->result = make_float2(r, ok ? 1.0f : 0.0f);
+        }
     }
-    buf ^= 1;  // the next reduction writes the other buffer: one barrier per reduction
-    return certify_round(S, C, errk, out);
+    __syncthreads();
+    const float2 res = rs->result;
+    *out = res.x;
+    return res.y != 0.0f;
+}
+
+// h' = bf16(RN32(a + b)) for BF16 a, b, as one packed BF16 add (a single
+// rounding of the exact sum). Same result: if the exponents of a and b differ
+// by at most 15, a + b fits in 24 bits and RN32 is exact; otherwise
+// |b| < 2^-15 |a|, far below half a BF16 ulp of a, and both roundings return a
+// (no tie is reachable). Infinities and NaN propagate alike.
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 __device__ __forceinline__ float rms_factor(float S, int D, float eps) {
@@ -115,21 +166,144 @@ __device__ __forceinline__ float rms_factor(float S, int D, float eps) {
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
-template <int VPT, bool MOE>
-__global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryParams p) {
-    __shared__ float2 red[2][32];
-    __shared__ ExactScratch sc;
+// Norm weights as FP32 pairs, staged once per CTA in shared memory by FULL
+// kernels: ws[j] = post_w[j], ws[D + j] = pre_w[j]. Other kernels read the
+// BF16 weights from global memory (L1-cached) on every row.
+__device__ __forceinline__ void stage_weights(const BoundaryParams& p, float* ws) {
+    for (int vi = threadIdx.x; vi < p.nvec; vi += blockDim.x) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(p.post_w) + vi);
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(p.pre_w) + vi);
+        float4* dp = reinterpret_cast<float4*>(ws) + 2 * vi;
+        float4* dq = reinterpret_cast<float4*>(ws + p.D) + 2 * vi;
+        float2 a0 = bf2_to_f2(a.x), a1 = bf2_to_f2(a.y), a2 = bf2_to_f2(a.z), a3 = bf2_to_f2(a.w);
+        float2 b0 = bf2_to_f2(b.x), b1 = bf2_to_f2(b.y), b2 = bf2_to_f2(b.z), b3 = bf2_to_f2(b.w);
+        dp[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
+        dp[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
+        dq[0] = make_float4(b0.x, b0.y, b1.x, b1.y);
+        dq[1] = make_float4(b2.x, b2.y, b3.x, b3.y);
+    }
+    __syncthreads();
+}
+
+// the 8 weights of vector vi as 4 FP32 pairs
+template <bool FULL>
+__device__ __forceinline__ void load_weights(const uint16_t* g, const float* ws, int vi, float2 (&w)[4]) {
+    if (FULL) {
+        const float4* p4 = reinterpret_cast<const float4*>(ws) + 2 * vi;
+        const float4 a = p4[0], b = p4[1];
+        w[0] = make_float2(a.x, a.y);
+        w[1] = make_float2(a.z, a.w);
+        w[2] = make_float2(b.x, b.y);
+        w[3] = make_float2(b.z, b.w);
+    } else {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(g) + vi);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = bf2_to_f2(word(v, q));
+    }
+}
+
+// Everything after the branch x and the stream h of a row are in registers:
+// post-norm sum, xn, residual (h' stored over h), pre-norm sum, y (stored).
+// `after_s1` runs on every thread right after the post-norm reduction's
+// barrier, when every thread has consumed its inputs of this row. FULL: the
+// row is exactly NT * VPT vectors (no bounds checks) and ws holds the weights.
+template <int VPT, bool MOE, bool FULL, class AfterS1>
+__device__ __forceinline__ void finish_row(const BoundaryParams& p, long long row, uint4 (&xv)[VPT],
+                                           uint4 (&hv)[VPT], RedScratch* rs, ExactScratch* sc,
+                                           const float* ws, AfterS1 after_s1) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const bool force_exact = (p.flags & kFlagForceExact) != 0;
+    const size_t base = (size_t)row * (size_t)p.D;
     const float2 c1 = make_float2(p.c1, p.c1), c2 = make_float2(p.c2, p.c2);
-    int buf = 0;
+
+    // ---- post-norm sum; the exact path reads x from global memory: the
+    // input row (dense) or, for MoE, the combined x parked in this y row
+    float S1;
+    const bool ok1 = block_sum_squares<VPT>(xv, p.errk, rs, &S1);
+    after_s1();
+    if (!ok1 || force_exact) {
+        const uint16_t* srow = p.x + base;
+        if (MOE) {
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int vi = tid + i * nt;
+                if (FULL || vi < p.nvec) st_stream(p.y + base + (size_t)vi * 8, xv[i]);
+            }
+            __syncthreads();
+            srow = p.y + base;
+        }
+        S1 = exact_row_sum_squares(srow, p.D, sc);
+    }
+    const float r1 = rms_factor(S1, p.D, p.eps);
+    const float2 r1v = make_float2(r1, r1);
+
+    // ---- xn, depth-scaled residual, store h' over h
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int vi = tid + i * nt;
+        if (FULL || vi < p.nvec) {
+            float2 pw[4];
+            load_weights<FULL>(p.post_w, ws, vi, pw);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float2 xf = bf2_to_f2(word(xv[i], q));
+                float2 xn = bf2_to_f2(f2_to_bf2(__fmul2_rn(__fmul2_rn(xf, r1v), pw[q])));
+                uint32_t a = f2_to_bf2(__fmul2_rn(c1, bf2_to_f2(word(hv[i], q))));
+                uint32_t b = f2_to_bf2(__fmul2_rn(c2, xn));
+                set_word(hv[i], q, bf2_add(a, b));
+            }
+            st_stream(p.h + base + (size_t)vi * 8, hv[i]);
+        }
+    }
+
+    // ---- pre-norm sum of h' (the exact path re-reads the h row just stored)
+    float S2;
+    if (!block_sum_squares<VPT>(hv, p.errk, rs, &S2) || force_exact)
+        S2 = exact_row_sum_squares(p.h + base, p.D, sc);
+    const float r2 = rms_factor(S2, p.D, p.eps);
+    const float2 r2v = make_float2(r2, r2);
+
+    // ---- y = bf16((h' r2) pre_w)
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int vi = tid + i * nt;
+        if (FULL || vi < p.nvec) {
+            float2 qw[4];
+            load_weights<FULL>(p.pre_w, ws ? ws + p.D : nullptr, vi, qw);
+            uint4 yv;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                set_word(yv, q, f2_to_bf2(__fmul2_rn(__fmul2_rn(bf2_to_f2(word(hv[i], q)), r2v), qw[q])));
+            st_stream(p.y + base + (size_t)vi * 8, yv);
+        }
+    }
+}
+
+struct NoOp {
+    __device__ void operator()() const {}
+};
+
+// Loads straight to registers (dense x or the MoE combine), optionally asking
+// L2 for the inputs of this CTA's row `prefetch_rows` ahead.
+template <int VPT, bool MOE, bool FULL>
+__global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryParams p) {
+    extern __shared__ __align__(16) float ws_dyn[];
+    __shared__ RedScratch rs;
+    __shared__ ExactScratch sc;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const float* ws = FULL ? ws_dyn : nullptr;
+
+    if (tid == 0)
+        for (int k = 1; k < p.prefetch_rows; ++k) prefetch_row<MOE>(p, blockIdx.x + (long long)k * gridDim.x);
+    if (FULL) stage_weights(p, ws_dyn);
 
     for (long long row = blockIdx.x; row < p.T; row += gridDim.x) {
         const size_t base = (size_t)row * (size_t)p.D;
         uint4 xv[VPT], hv[VPT];
+        if (tid == 0 && p.prefetch_rows > 0) prefetch_row<MOE>(p, row + (long long)p.prefetch_rows * gridDim.x);
 
-        // ---- branch output x (dense: load; MoE: FP32 fma chain over the 8 experts)
         if (MOE) {
+            // x = bf16(fma chain over the 8 experts, k ascending)
             const float4 wa = __ldg(reinterpret_cast<const float4*>(p.w + row * kTopK));
             const float4 wb = __ldg(reinterpret_cast<const float4*>(p.w + row * kTopK + 4));
             const float wk[kTopK] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
@@ -145,7 +319,7 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
 #pragma unroll
                 for (int i = 0; i < VPT; ++i) {
                     const int vi = tid + i * nt;
-                    if (vi < p.nvec) {
+                    if (FULL || vi < p.nvec) {
                         uint4 ev = ld_stream_ro(erow + (size_t)k * p.D + (size_t)vi * 8);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
@@ -161,74 +335,90 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int vi = tid + i * nt;
-                xv[i] = vi < p.nvec ? ld_stream_ro(p.x + base + (size_t)vi * 8) : make_uint4(0, 0, 0, 0);
+                xv[i] = (FULL || vi < p.nvec) ? ld_stream_ro(p.x + base + (size_t)vi * 8) : make_uint4(0, 0, 0, 0);
             }
         }
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int vi = tid + i * nt;
-            hv[i] = vi < p.nvec ? ld_stream_rw(p.h + base + (size_t)vi * 8) : make_uint4(0, 0, 0, 0);
+            hv[i] = (FULL || vi < p.nvec) ? ld_stream_rw(p.h + base + (size_t)vi * 8) : make_uint4(0, 0, 0, 0);
         }
-
-        // ---- post-norm sum; the exact path reads x from global memory: the
-        // input row (dense) or, for MoE, the combined x parked in this y row
-        float S1;
-        if (!block_sum_squares<VPT>(xv, p.errk, red, buf, &S1) || force_exact) {
-            const uint16_t* srow = p.x + base;
-            if (MOE) {
-#pragma unroll
-                for (int i = 0; i < VPT; ++i) {
-                    const int vi = tid + i * nt;
-                    if (vi < p.nvec) st_stream(p.y + base + (size_t)vi * 8, xv[i]);
-                }
-                __syncthreads();
-                srow = p.y + base;
-            }
-            S1 = exact_row_sum_squares(srow, p.D, &sc);
-        }
-        const float r1 = rms_factor(S1, p.D, p.eps);
-        const float2 r1v = make_float2(r1, r1);
-
-        // ---- xn, depth-scaled residual, store h' over h
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            const int vi = tid + i * nt;
-            if (vi < p.nvec) {
-                const uint4 pw = __ldg(reinterpret_cast<const uint4*>(p.post_w) + vi);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float2 xf = bf2_to_f2(word(xv[i], q));
-                    float2 xn = bf2_to_f2(f2_to_bf2(__fmul2_rn(__fmul2_rn(xf, r1v), bf2_to_f2(word(pw, q)))));
-                    float2 a = bf2_to_f2(f2_to_bf2(__fmul2_rn(c1, bf2_to_f2(word(hv[i], q)))));
-                    float2 b = bf2_to_f2(f2_to_bf2(__fmul2_rn(c2, xn)));
-                    set_word(hv[i], q, f2_to_bf2(__fadd2_rn(a, b)));
-                }
-                st_stream(p.h + base + (size_t)vi * 8, hv[i]);
-            }
-        }
-
-        // ---- pre-norm sum of h' (the exact path re-reads the h row just stored)
-        float S2;
-        if (!block_sum_squares<VPT>(hv, p.errk, red, buf, &S2) || force_exact)
-            S2 = exact_row_sum_squares(p.h + base, p.D, &sc);
-        const float r2 = rms_factor(S2, p.D, p.eps);
-        const float2 r2v = make_float2(r2, r2);
-
-        // ---- y = bf16((h' r2) pre_w)
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            const int vi = tid + i * nt;
-            if (vi < p.nvec) {
-                const uint4 qw = __ldg(reinterpret_cast<const uint4*>(p.pre_w) + vi);
-                uint4 yv;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    set_word(yv, q, f2_to_bf2(__fmul2_rn(__fmul2_rn(bf2_to_f2(word(hv[i], q)), r2v),
-                                                         bf2_to_f2(word(qw, q)))));
-                st_stream(p.y + base + (size_t)vi * 8, yv);
-            }
-        }
+        finish_row<VPT, MOE, FULL>(p, row, xv, hv, &rs, &sc, ws, NoOp{});
     }
+}
+
+// Dense boundary fed by a ring of `stages` shared-memory slots per CTA. Slot s
+// holds [x row | h row] of one of this CTA's rows (rows blockIdx.x + i*gridDim.x,
+// slot i % stages), filled by two 1-D bulk copies that complete on the slot's
+// mbarrier. One thread refills a slot with the row `stages` ahead as soon as
+// the post-norm reduction's barrier shows every thread has read it, so up to
+// stages-1 rows per CTA are in flight while a row is computed. FULL kernels
+// keep the FP32 weights after the ring.
+template <int VPT, bool FULL>
+__global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const BoundaryParams p) {
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ __align__(8) uint64_t test_bar;
+    __shared__ RedScratch rs;
+    __shared__ ExactScratch sc;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int S = p.stages;
+    const uint32_t row_bytes = (uint32_t)p.D * 2u;
+    const long long G = gridDim.x;
+    const long long n_iter = (p.T - blockIdx.x + G - 1) / G;  // grid <= T: at least one row
+    float* ws = FULL ? reinterpret_cast<float*>(ring + (size_t)S * 2u * row_bytes) : nullptr;
+
+    auto slot_x = [&](int s) { return ring + (size_t)s * 2u * row_bytes; };
+    auto issue = [&](long long i) {  // thread 0 only
+        const int s = (int)(i % S);
+        const size_t off = (size_t)(blockIdx.x + i * G) * (size_t)p.D;
+        mbar_arrive_expect_tx(&full[s], 2u * row_bytes);
+        bulk_load(slot_x(s), p.x + off, row_bytes, &full[s]);
+        bulk_load(slot_x(s) + row_bytes, p.h + off, row_bytes, &full[s]);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        mbar_init(&test_bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (long long i = 0; i < S && i < n_iter; ++i) issue(i);
+    if (FULL) stage_weights(p, ws);
+
+    // test hook: wait on a barrier that nothing completes; it must run out
+    if ((p.flags & kFlagTestWaitTimeout) && !mbar_wait_bounded(&test_bar, 0, p.test_wait_ns) && tid == 0)
+        report_timeout();
+
+    bool dead = false;             // a wait of this thread gave up: skip later waits and refills
+    long long dead_from = n_iter;  // first iteration whose copies thread 0 did not see complete
+    for (long long i = 0; i < n_iter; ++i) {
+        const int s = (int)(i % S);
+        const uint32_t parity = (uint32_t)((i / S) & 1);
+        if (!dead && !mbar_wait_bounded(&full[s], parity, p.wait_ns)) {
+            dead = true;
+            dead_from = i;
+            report_timeout();
+        }
+        const uint4* xs = reinterpret_cast<const uint4*>(slot_x(s));
+        const uint4* hs = reinterpret_cast<const uint4*>(slot_x(s) + row_bytes);
+        uint4 xv[VPT], hv[VPT];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int vi = tid + j * nt;
+            xv[j] = (FULL || vi < p.nvec) ? xs[vi] : make_uint4(0, 0, 0, 0);
+            hv[j] = (FULL || vi < p.nvec) ? hs[vi] : make_uint4(0, 0, 0, 0);
+        }
+        finish_row<VPT, false, FULL>(p, blockIdx.x + i * G, xv, hv, &rs, &sc, ws, [&]() {
+            if (tid == 0 && !dead && i + S < n_iter) issue(i + S);
+        });
+    }
+    // a slot copy that timed out may still land: wait (bounded) before the
+    // CTA's shared memory is released
+    if (tid == 0 && dead)
+        for (long long i = dead_from; i < n_iter && i < dead_from + S; ++i)
+            mbar_wait_bounded(&full[i % S], (uint32_t)((i / S) & 1), p.wait_ns);
 }
 
 }  // namespace beam

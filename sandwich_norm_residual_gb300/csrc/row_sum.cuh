@@ -14,6 +14,7 @@
 // it depends on the terms per thread and the merge depth). The rounding of
 // s + c is certified when [s + c - E, s + c + E] lies strictly inside the
 // rounding interval of RN32(s + c); about one row sum in 10^4 is not, and then
+// the exact path decides.
 //
 // Exact path (rare, or forced): the row is re-read from global memory and the
 // sum is formed exactly as a 320-bit integer (each FP32 term is m * 2^q *
@@ -40,23 +41,16 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
     return d;
 }
 
-__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
-    unsigned long long ua, ub, ud;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(ud) : "l"(ua), "l"(ub));
-    float2 d;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
-    return d;
-}
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
 
 // s + c += t, error-free on (s, e) and accumulated into c, both lanes at once
+// (negation is an operand modifier of the packed add)
 __device__ __forceinline__ void two_sum_acc2(float2& s, float2& c, float2 t) {
     float2 sn = __fadd2_rn(s, t);
-    float2 bp = fsub2(sn, s);
-    float2 ap = fsub2(sn, bp);
-    float2 db = fsub2(t, bp);
-    float2 da = fsub2(s, ap);
+    float2 bp = __fadd2_rn(sn, neg2(s));
+    float2 ap = __fadd2_rn(sn, neg2(bp));
+    float2 db = __fadd2_rn(t, neg2(bp));
+    float2 da = __fadd2_rn(s, neg2(ap));
     c = __fadd2_rn(c, __fadd2_rn(da, db));
     s = sn;
 }

@@ -55,7 +55,7 @@ def test_header_constants_match_binding():
         assert getattr(_lib, name) == int(val), name
     assert _lib.BEAM_MAX_D == int(re.search(r"#define BEAM_MAX_D (\d+)", text).group(1))
     assert _lib.BEAM_MOE_TOPK == int(re.search(r"#define BEAM_MOE_TOPK (\d+)", text).group(1))
-    assert ctypes.sizeof(_lib.LaunchOpts) == 16
+    assert ctypes.sizeof(_lib.LaunchOpts) == 32
 
 
 def test_version_and_status_strings(lib):
@@ -131,6 +131,24 @@ def test_bad_launch_options_are_rejected(lib):
     assert lib.beam_moe_combine_boundary_ex(None, A, A + (1 << 32), A + (5 << 32), A + (2 << 32),
                                             A + (3 << 32), 2, 1e-6, 4, 8192, A + (4 << 32),
                                             ctypes.byref(opts)) == _lib.BEAM_ERR_ARG
+
+
+def _dense_ex(lib, **kw):
+    opts = _lib.LaunchOpts(**kw)
+    return lib.beam_boundary_fused_ex(None, A, A + (1 << 32), A + (2 << 32), A + (3 << 32), 2,
+                                      1e-6, 4, D, A + (4 << 32), ctypes.byref(opts))
+
+
+def test_bad_ring_options_are_rejected(lib):
+    assert _dense_ex(lib, stages=1) == _lib.BEAM_ERR_ARG
+    assert _dense_ex(lib, stages=9) == _lib.BEAM_ERR_ARG
+    assert _dense_ex(lib, stages=-2) == _lib.BEAM_ERR_ARG
+    assert _dense_ex(lib, prefetch_rows=9) == _lib.BEAM_ERR_ARG
+    assert _dense_ex(lib, prefetch_rows=-2) == _lib.BEAM_ERR_ARG
+    r = (ctypes.c_int32 * 3)(0, 1, 0)
+    assert _dense_ex(lib, reserved=r) == _lib.BEAM_ERR_ARG
+    # the wait test hook needs the ring kernel
+    assert _dense_ex(lib, flags=_lib.BEAM_OPT_TEST_WAIT_TIMEOUT, stages=-1) == _lib.BEAM_ERR_ARG
 
 
 def test_exact_count_rejects_null(lib):

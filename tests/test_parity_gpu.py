@@ -238,13 +238,54 @@ def test_launch_shape_does_not_change_a_bit():
     T, D = 200, 5120
     inp = random_dense(T, D, seed=10)
     ref = None
-    for vpt in (2, 3, 4, 5, 6, 7, 8):  # one vector per thread would need 640 threads
-        for per_sm in (0, 1):
-            got = gpu_dense(inp, 11, 1e-6, opts=dict(vec_per_thread=vpt, ctas_per_sm=per_sm))
-            if ref is None:
-                ref = got
-                check(got, oracle_dense(inp, 11, 1e-6), "vpt sweep reference")
-            assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), (vpt, per_sm)
+    shapes = [dict(vec_per_thread=v, ctas_per_sm=c, stages=st)
+              for v in (2, 3, 4, 5, 6, 7, 8)  # one vector per thread would need 640 threads
+              for c in (0, 1) for st in (-1, 0)]
+    shapes += [dict(vec_per_thread=5, stages=st, ctas_per_sm=c) for st in (2, 3, 5, 8)
+               for c in (0, 1, 3)]
+    shapes += [dict(stages=-1, prefetch_rows=pf) for pf in (-1, 1, 4)]
+    for opts in shapes:
+        got = gpu_dense(inp, 11, 1e-6, opts=opts)
+        if ref is None:
+            ref = got
+            check(got, oracle_dense(inp, 11, 1e-6), "launch-shape sweep reference")
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), opts
+
+
+def test_moe_launch_shape_does_not_change_a_bit():
+    cfg = CONFIGS[3]
+    m = synth.moe_inputs(cfg, rows=96)
+    ref = gpu_moe(m, cfg.n, cfg.eps)
+    check(ref, oracle_moe(m, cfg.n, cfg.eps), "moe launch-shape reference")
+    for v in (2, 3, 4, 5, 8):
+        for pf in (-1, 1, 3):
+            got = gpu_moe(m, cfg.n, cfg.eps, opts=dict(vec_per_thread=v, prefetch_rows=pf))
+            assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), (v, pf)
+
+
+def test_ring_kernel_at_a_hidden_size_where_fewer_slots_fit():
+    # 4 * D bytes per slot: D = 16384 leaves room for three slots, D = 32768 for none
+    for T, D in ((40, 16384), (5, 32768)):
+        inp = random_dense(T, D, seed=D)
+        check(gpu_dense(inp, 3, 1e-6), oracle_dense(inp, 3, 1e-6), f"ring D={D}")
+
+
+def test_bounded_wait_runs_out_reports_timeout_and_leaves_the_context_usable():
+    """The test hook makes every CTA wait on an mbarrier that nothing completes;
+    each wait gives up after 1 ms and the status word reports it."""
+    T, D = 64, 5120
+    inp = random_dense(T, D, seed=16)
+    d = to_dev(inp)
+    opts = dict(flags=snr._lib.BEAM_OPT_TEST_WAIT_TIMEOUT)
+    y = snr.boundary_fused(d["h"], d["x"], d["post_w"], d["pre_w"], 5, 1e-6, opts=opts)
+    with pytest.raises(snr.BeamError) as ei:
+        snr.sync_status()
+    assert ei.value.status == snr._lib.BEAM_ERR_TIMEOUT
+    # the launch carried on: results are still exact
+    check((bits(d["h"]), bits(y)), oracle_dense(inp, 5, 1e-6), "after a timed-out wait")
+    # the status was cleared and the context still works
+    snr.sync_status()
+    check(gpu_dense(inp, 5, 1e-6), oracle_dense(inp, 5, 1e-6), "next call")
 
 
 def test_forced_exact_path_is_bit_identical_and_counted():
