@@ -35,7 +35,12 @@ METRIC = "fused boundary tokens/s at T=16384 (dense + MoE boundary of one decode
 
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {}  # kernel -> {"bytes_per_launch": B, "source_sha": sha, "profile": path}
+NCU_TRAFFIC = {
+    "moe": {"bytes_per_launch": 1_517_829_000 + 292_617_472, "source_sha": "1c5a310e065f4617",
+            "profile": "profiles/moe_combine_boundary_T16384.md"},
+    "dense": {"bytes_per_launch": 335_669_000 + 275_125_760, "source_sha": "1c5a310e065f4617",
+              "profile": "profiles/dense_boundary_T16384.md"},
+}
 
 
 def kernel_source_sha() -> str:

@@ -104,13 +104,14 @@ struct RedScratch {
 // Block-wide compensated sum of the squares of the row held in v[] (zeros in
 // unused slots). Every thread folds its two FP32 lanes into one pair and
 // stores it; warp 0 merges the pairs (lane l takes l, l+32, ... in order, then
-// a 5-level xor butterfly), certifies the rounding and broadcasts it. Returns
-// true with *out = RN32(exact sum) when certified; false when the exact path
-// must decide. The first barrier also orders every store this block issued
-// before the call ahead of any load after it (the exact path re-reads rows).
-template <int VPT>
+// a 5-level xor butterfly), certifies the rounding and broadcasts it. The
+// other warps run `overlap` while warp 0 merges; warp 0 runs it afterwards.
+// Returns true with *out = RN32(exact sum) when certified; false when the
+// exact path must decide. The first barrier also orders every store this
+// block issued before the call ahead of any load after it.
+template <int VPT, class Overlap>
 __device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float errk, RedScratch* rs,
-                                                  float* out) {
+                                                  float* out, Overlap overlap) {
     float2 s = make_float2(0.f, 0.f), c = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
@@ -123,7 +124,8 @@ __device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float e
     ff_merge(S, C, s.y, c.y);
     rs->part[threadIdx.x] = make_float2(S, C);
     __syncthreads();
-    if (threadIdx.x < 32) {
+    const bool merger = threadIdx.x < 32;
+    if (merger) {
         const int nw = blockDim.x >> 5;
         float2 t0 = rs->part[threadIdx.x];
         S = t0.x;
@@ -143,8 +145,11 @@ __device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float e
             bool ok = certify_round(S, C, errk, &r);
             rs->result = make_float2(r, ok ? 1.0f : 0.0f);
         }
+    } else {
+        overlap();
     }
     __syncthreads();
+    if (merger) overlap();
     const float2 res = rs->result;
     *out = res.x;
     return res.y != 0.0f;
@@ -216,12 +221,21 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
     const size_t base = (size_t)row * (size_t)p.D;
     const float2 c1 = make_float2(p.c1, p.c1), c2 = make_float2(p.c2, p.c2);
 
-    // ---- post-norm sum; the exact path reads x from global memory: the
-    // input row (dense) or, for MoE, the combined x parked in this y row
+    // ---- post-norm sum; while warp 0 merges, the others scale the stream:
+    // a = bf16(c1 h) replaces h in registers (it does not depend on r1)
+    auto scale_stream = [&]() {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                set_word(hv[i], q, f2_to_bf2(__fmul2_rn(c1, bf2_to_f2(word(hv[i], q)))));
+    };
     float S1;
-    const bool ok1 = block_sum_squares<VPT>(xv, p.errk, rs, &S1);
+    const bool ok1 = block_sum_squares<VPT>(xv, p.errk, rs, &S1, scale_stream);
     after_s1();
     if (!ok1 || force_exact) {
+        // the exact path reads x from global memory: the input row (dense)
+        // or, for MoE, the combined x parked in this y row
         const uint16_t* srow = p.x + base;
         if (MOE) {
 #pragma unroll
@@ -237,7 +251,7 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
     const float r1 = rms_factor(S1, p.D, p.eps);
     const float2 r1v = make_float2(r1, r1);
 
-    // ---- xn, depth-scaled residual, store h' over h
+    // ---- xn, b = bf16(c2 xn), h' = a + b (in registers)
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int vi = tid + i * nt;
@@ -248,18 +262,27 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
             for (int q = 0; q < 4; ++q) {
                 float2 xf = bf2_to_f2(word(xv[i], q));
                 float2 xn = bf2_to_f2(f2_to_bf2(__fmul2_rn(__fmul2_rn(xf, r1v), pw[q])));
-                uint32_t a = f2_to_bf2(__fmul2_rn(c1, bf2_to_f2(word(hv[i], q))));
                 uint32_t b = f2_to_bf2(__fmul2_rn(c2, xn));
-                set_word(hv[i], q, bf2_add(a, b));
+                set_word(hv[i], q, bf2_add(word(hv[i], q), b));
             }
-            st_stream(p.h + base + (size_t)vi * 8, hv[i]);
+        } else {
+            hv[i] = make_uint4(0, 0, 0, 0);
         }
     }
 
-    // ---- pre-norm sum of h' (the exact path re-reads the h row just stored)
+    // ---- pre-norm sum of h'; h' is stored over h while warp 0 merges
+    auto store_stream = [&]() {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int vi = tid + i * nt;
+            if (FULL || vi < p.nvec) st_stream(p.h + base + (size_t)vi * 8, hv[i]);
+        }
+    };
     float S2;
-    if (!block_sum_squares<VPT>(hv, p.errk, rs, &S2) || force_exact)
+    if (!block_sum_squares<VPT>(hv, p.errk, rs, &S2, store_stream) || force_exact) {
+        __syncthreads();  // warp 0 stored its part of h' after the reduction's last barrier
         S2 = exact_row_sum_squares(p.h + base, p.D, sc);
+    }
     const float r2 = rms_factor(S2, p.D, p.eps);
     const float2 r2v = make_float2(r2, r2);
 

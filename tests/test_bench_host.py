@@ -1,0 +1,92 @@
+"""Host-side logic of bench.py on CPU: row shards, the max-over-ranks timing
+reduction with two gloo ranks, and the reference arm's JSON line."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_shard_rows_cover_the_batch_once():
+    for total in (0, 1, 7, 16384, 131071):
+        for world in (1, 2, 3, 8):
+            parts = [bench.shard_rows(total, r, world) for r in range(world)]
+            assert parts[0][0] == 0 and parts[-1][1] == total
+            for (a, b), (c, d) in zip(parts, parts[1:]):
+                assert b == c and a <= b
+            sizes = [b - a for a, b in parts]
+            assert max(sizes) - min(sizes) <= 1
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks(10.0 + rank)
+        bench.barrier()
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=5) for _ in range(2))
+    assert res == {0: 11.0, 1: 11.0}
+
+
+def test_max_over_ranks_without_a_process_group_is_identity():
+    assert bench.max_over_ranks(3.5) == 3.5
+
+
+def _run_bench(args, env_extra=None):
+    env = dict(os.environ, **(env_extra or {}))
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, cwd=ROOT,
+                          env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = _run_bench(["--impl", "reference", "--steps", "2", "--warmup", "1", "--ref-rows", "2"])
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_reference_arm_is_silent_on_other_ranks():
+    r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0"],
+                   {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_bench_byte_counts():
+    D = bench.D
+    assert bench.dense_bytes(16384) == 16384 * 8 * D + 4 * D == 671_109_120
+    assert bench.moe_bytes(16384) == 16384 * (22 * D + 32) + 4 * D == 1_846_038_528
