@@ -186,6 +186,71 @@ def run_step(snr, d, stream):
                              MOE_N, EPS, y=mo["y"], stream=stream)
 
 
+def decode_latency(snr, device, replays: int = 20) -> dict:
+    """Decode-size boundaries, launch-bound: CUDA-graph replays, with and without
+    programmatic dependent launch (PDL). T = 4: microseconds per boundary over
+    200 captured calls. T = 64: microseconds per 104-boundary chain (n = 2..105,
+    fresh x and weights per boundary)."""
+    import torch
+    import synth
+    from synth import CONFIGS
+    out = {}
+    stream = torch.cuda.Stream(device)
+    pdl_opts = {False: None, True: dict(flags=snr._lib.BEAM_OPT_PDL)}
+
+    def timed_graph(body, label, reps):
+        with torch.cuda.stream(stream):
+            body()  # first calls set up the launch shapes outside the capture
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):  # replays run on the current stream
+            g.replay()
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) * 1e3 / reps
+
+    c0 = CONFIGS[0]
+    d0 = {k: v.to(device) for k, v in synth.dense_inputs(c0).items()}
+    y0 = torch.empty_like(d0["h"])
+    for pdl in (False, True):
+        def body0(pdl=pdl):
+            for _ in range(200):
+                snr.boundary_fused(d0["h"], d0["x"], d0["post_w"], d0["pre_w"], c0.n, c0.eps, y=y0,
+                                   opts=pdl_opts[pdl], stream=stream)
+        out[f"T4_us_per_boundary{'_pdl' if pdl else ''}"] = timed_graph(body0, "t4", replays) / 200
+
+    c1 = CONFIGS[1]
+    h1 = synth.dense_inputs(c1)["h"].to(device)
+    steps = [{k: v.to(device) for k, v in synth.dense_inputs(c1, step=s).items()}
+             for s in range(c1.steps)]
+    ys = torch.empty((c1.steps,) + tuple(h1.shape), dtype=h1.dtype, device=device)
+    for pdl in (False, True):
+        def body1(pdl=pdl):
+            for s, d in enumerate(steps):
+                snr.boundary_fused(h1, d["x"], d["post_w"], d["pre_w"], c1.n + s, c1.eps, y=ys[s],
+                                   opts=pdl_opts[pdl], stream=stream)
+        out[f"chain104_T64_us{'_pdl' if pdl else ''}"] = timed_graph(body1, "chain", replays)
+    # the same chain launched one call at a time, no graph
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(replays):
+            for s, d in enumerate(steps):
+                snr.boundary_fused(h1, d["x"], d["post_w"], d["pre_w"], c1.n + s, c1.eps, y=ys[s],
+                                   stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    out["chain104_T64_us_stream_launches"] = a.elapsed_time(b) * 1e3 / replays
+    snr.sync_status(stream)
+    return {k: round(v, 2) for k, v in out.items()}
+
+
 def bench_ours(args, rank, world, local_rank):
     import torch
     import sandwich_norm_residual_gb300 as snr
@@ -319,6 +384,8 @@ def bench_ours(args, rank, world, local_rank):
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
+    if not args.no_decode:
+        line["config"]["decode"] = decode_latency(snr, device)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -401,6 +468,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-size latency figures")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
     if args.impl == "reference":

@@ -165,6 +165,14 @@ typedef struct {
  * 1 ms, the device status word records it (beam_sync_status then returns
  * BEAM_ERR_TIMEOUT) and the launch carries on normally. */
 #define BEAM_OPT_TEST_WAIT_TIMEOUT 0x2u
+/* Programmatic dependent launch (the following norm loads its weights before
+ * its dependency wait: SGLang page, "Fusion optimizations"). The kernel may
+ * start while the previous kernel on the stream is still running: it reads
+ * post_w and pre_w, then waits for that kernel to finish before it touches h,
+ * x, expert_out or topk_w, and lets the next kernel start its own prologue
+ * early. Use it only when the kernels just before this call on the stream do
+ * not write post_w or pre_w. */
+#define BEAM_OPT_PDL 0x4u
 
 BEAM_API beam_status beam_boundary_fused_ex(beam_stream_t stream, uint16_t* h, const uint16_t* x,
                                    const uint16_t* post_w, const uint16_t* pre_w, int n,

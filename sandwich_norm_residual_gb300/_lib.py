@@ -21,6 +21,7 @@ BEAM_MAX_D = 32768
 BEAM_MOE_TOPK = 8
 BEAM_OPT_FORCE_EXACT_SUM = 0x1
 BEAM_OPT_TEST_WAIT_TIMEOUT = 0x2
+BEAM_OPT_PDL = 0x4
 
 
 class LaunchOpts(ctypes.Structure):

@@ -229,7 +229,7 @@ beam_status check_common(int n, float eps, int64_t T, int D, const beam_launch_o
         if (opts->vec_per_thread < 0 || opts->vec_per_thread > kMaxVpt || opts->ctas_per_sm < 0 ||
             opts->prefetch_rows < -1 || opts->prefetch_rows > kMaxPrefetch || opts->stages < -1 ||
             opts->stages == 1 || opts->stages > beam::kMaxStages || opts->reserved[0] || opts->reserved[1] ||
-            opts->reserved[2] || (opts->flags & ~(BEAM_OPT_FORCE_EXACT_SUM | BEAM_OPT_TEST_WAIT_TIMEOUT)))
+            opts->reserved[2] || (opts->flags & ~(BEAM_OPT_FORCE_EXACT_SUM | BEAM_OPT_TEST_WAIT_TIMEOUT | BEAM_OPT_PDL)))
             return BEAM_ERR_ARG;
         if ((opts->flags & BEAM_OPT_TEST_WAIT_TIMEOUT) && opts->stages == -1) return BEAM_ERR_ARG;
         if (opts->vec_per_thread && !threads_for(D / 8, opts->vec_per_thread)) return BEAM_ERR_ARG;
@@ -327,8 +327,25 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
     p.test_wait_ns = kTestWaitNs;
 
     void* args[] = {&p};
-    cudaError_t err = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3((unsigned)grid), dim3(nt), args,
-                                       (size_t)smem, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t err;
+    if (opts && (opts->flags & BEAM_OPT_PDL)) {
+        // programmatic dependent launch: the kernel may start during the
+        // previous kernel on the stream and waits for it after staging weights
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(nt);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
+    } else {
+        err = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3((unsigned)grid), dim3(nt), args,
+                               (size_t)smem, reinterpret_cast<cudaStream_t>(stream));
+    }
     if (err != cudaSuccess) {
         cudaGetLastError();
         return BEAM_ERR_CUDA;

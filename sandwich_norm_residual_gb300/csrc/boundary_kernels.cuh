@@ -72,6 +72,14 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialisation may start while the previous kernel on the stream still runs;
+// pdl_wait() returns once that kernel has completed and its writes are
+// visible (at once when the launch had no such dependency). pdl_trigger()
+// lets the next kernel on the stream start its own prologue early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16)
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
@@ -316,9 +324,14 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
     const int tid = threadIdx.x, nt = blockDim.x;
     const float* ws = FULL ? ws_dyn : nullptr;
 
+    // prologue that reads only the norm weights; with a programmatic launch it
+    // overlaps the previous kernel on the stream (the caller guarantees that
+    // kernel does not write the weights)
+    pdl_trigger();
+    if (FULL) stage_weights(p, ws_dyn);
+    pdl_wait();
     if (tid == 0)
         for (int k = 1; k < p.prefetch_rows; ++k) prefetch_row<MOE>(p, blockIdx.x + (long long)k * gridDim.x);
-    if (FULL) stage_weights(p, ws_dyn);
 
     for (long long row = blockIdx.x; row < p.T; row += gridDim.x) {
         const size_t base = (size_t)row * (size_t)p.D;
@@ -406,9 +419,11 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const Bounda
         mbar_fence_init();
     }
     __syncthreads();
+    pdl_trigger();
+    if (FULL) stage_weights(p, ws);  // weights only: may overlap the previous kernel
+    pdl_wait();
     if (tid == 0)
         for (long long i = 0; i < S && i < n_iter; ++i) issue(i);
-    if (FULL) stage_weights(p, ws);
 
     // test hook: wait on a barrier that nothing completes; it must run out
     if ((p.flags & kFlagTestWaitTimeout) && !mbar_wait_bounded(&test_bar, 0, p.test_wait_ns) && tid == 0)

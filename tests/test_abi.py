@@ -147,6 +147,8 @@ def test_bad_ring_options_are_rejected(lib):
     assert _dense_ex(lib, prefetch_rows=-2) == _lib.BEAM_ERR_ARG
     r = (ctypes.c_int32 * 3)(0, 1, 0)
     assert _dense_ex(lib, reserved=r) == _lib.BEAM_ERR_ARG
+    # programmatic dependent launch is a valid option (the call then reaches CUDA)
+    assert _dense_ex(lib, flags=_lib.BEAM_OPT_PDL) != _lib.BEAM_ERR_ARG
     # the wait test hook needs the ring kernel
     assert _dense_ex(lib, flags=_lib.BEAM_OPT_TEST_WAIT_TIMEOUT, stages=-1) == _lib.BEAM_ERR_ARG
 

@@ -359,3 +359,68 @@ def test_zero_tokens_is_a_no_op_and_streams_are_honoured():
     with torch.cuda.stream(s):
         got = gpu_dense(inp, 9, 1e-6, stream=s)
     check(got, oracle_dense(inp, 9, 1e-6), "side stream")
+
+
+# --------------------------------------------------------------- decode chain: graphs and PDL
+
+def _chain_inputs(cfg):
+    steps = [synth.dense_inputs(cfg, step=s) for s in range(cfg.steps)]
+    return synth.dense_inputs(cfg)["h"], steps
+
+
+@pytest.mark.parametrize("pdl", [False, True])
+@pytest.mark.parametrize("graph", [False, True])
+def test_decode_chain_with_cuda_graph_and_pdl_matches_the_oracle(pdl, graph):
+    """All 104 boundaries of the T = 64 decode chain back to back on one stream
+    (optionally captured in one CUDA graph, optionally with programmatic
+    dependent launches); every step's y and the final stream are exact."""
+    cfg = CONFIGS[1]
+    h0, steps = _chain_inputs(cfg)
+    dev_steps = [to_dev(s) for s in steps]
+    h = h0.to(DEV)
+    ys = [torch.empty_like(h) for _ in steps]
+    opts = dict(flags=snr._lib.BEAM_OPT_PDL) if pdl else None
+    stream = torch.cuda.Stream()
+
+    def run_chain():
+        for s, d in enumerate(dev_steps):
+            snr.boundary_fused(h, d["x"], d["post_w"], d["pre_w"], cfg.n + s, cfg.eps, y=ys[s],
+                               opts=opts, stream=stream)
+
+    with torch.cuda.stream(stream):
+        run_chain()  # first call on the device sets up the launch shapes (before any capture)
+    torch.cuda.synchronize()
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run_chain()
+        h.copy_(h0.to(DEV))
+        for y in ys:
+            y.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+    else:
+        h.copy_(h0.to(DEV))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            run_chain()
+    torch.cuda.synchronize()
+    snr.sync_status()
+
+    h_ref = oracle.as_u16(h0).copy()
+    for s, inp in enumerate(steps):
+        h_ref, y_ref = oracle.boundary(h_ref, inp["x"], inp["post_w"], inp["pre_w"], cfg.n + s,
+                                       cfg.eps, threads=THREADS)
+        assert_parity(bits(ys[s]), y_ref, f"chain step {s} y (graph={graph}, pdl={pdl})")
+    check((bits(h), bits(ys[-1])), (h_ref, y_ref), f"chain graph={graph} pdl={pdl}")
+
+
+def test_pdl_on_the_prefill_and_moe_workloads():
+    cfg = CONFIGS[2]
+    inp = synth.dense_inputs(cfg, rows=2048)
+    opts = dict(flags=snr._lib.BEAM_OPT_PDL)
+    check(gpu_dense(inp, cfg.n, cfg.eps, opts=opts), oracle_dense(inp, cfg.n, cfg.eps), "dense pdl")
+    m = synth.moe_inputs(CONFIGS[3], rows=512)
+    check(gpu_moe(m, 20, 1e-6, opts=opts), oracle_moe(m, 20, 1e-6), "moe pdl")
+    check(gpu_dense(inp, cfg.n, cfg.eps, opts=dict(flags=snr._lib.BEAM_OPT_PDL, stages=2)),
+          oracle_dense(inp, cfg.n, cfg.eps), "dense ring pdl")
