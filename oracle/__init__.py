@@ -74,6 +74,10 @@ def _load():
             lib.oracle_boundary_ld.restype = i32
             lib.oracle_residual_ld.argtypes = [vp, vp, i32, i64]
             lib.oracle_residual_ld.restype = None
+            lib.oracle_route.argtypes = [vp, vp, i64, i32, i32, i32, i32, f32, vp, vp]
+            lib.oracle_route.restype = i32
+            lib.oracle_sigmoid.argtypes = [f32]
+            lib.oracle_sigmoid.restype = f32
             _lib = lib
     return _lib
 
@@ -218,3 +222,29 @@ def residual_ld(h, x, n: int) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.longdouble)
     _load().oracle_residual_ld(_p(h), _p(x), n, h.size)
     return h
+
+
+def sigmoid(z: float) -> float:
+    return float(_load().oracle_sigmoid(z))
+
+
+def route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8,
+          scale: float = 2.5, threads: int = 1):
+    """Group-limited top-k routing; returns (idx int32 [T, topk], w float32 [T, topk])."""
+    z = np.ascontiguousarray(logits.numpy() if hasattr(logits, "numpy") else logits,
+                             dtype=np.float32)
+    b = np.ascontiguousarray(bias.numpy() if hasattr(bias, "numpy") else bias, dtype=np.float32)
+    T, E = z.shape
+    idx = np.empty((T, topk), np.int32)
+    w = np.empty((T, topk), np.float32)
+    lib = _load()
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        rc = lib.oracle_route(_p(z[lo:hi]), _p(b), hi - lo, E, n_group, topk_group, topk, scale,
+                              _p(idx[lo:hi]), _p(w[lo:hi]))
+        if rc != 0:
+            raise ValueError("oracle_route: bad arguments")
+
+    _run_rows(run, T, threads)
+    return idx, w

@@ -280,3 +280,90 @@ void oracle_residual_ld(long double* h, const long double* x, int n, int64_t cou
     long double c2 = 1.0L / sqrtl((long double)n);
     for (int64_t i = 0; i < count; ++i) h[i] = c1 * h[i] + c2 * x[i];
 }
+
+/* ------------------------------------------------------------------------
+ * Group-limited top-k routing in front of the MoE combine (vLLM page, "MoE
+ * and residual stream": sigmoid scores plus a correction bias pick the best
+ * 4 of 8 expert groups, then the top 8 experts, and the renormalised weights
+ * are scaled by 2.5; SGLang page, "Dense layers and grouped MoE routing":
+ * FP32 logits and routing coefficients; HF page: 8 groups of 32 experts).
+ *
+ * Per token, FP32 throughout:
+ *   s_e = RN32(1 / (1 + exp(-z_e)))       the sigmoid, correctly rounded
+ *                                         (evaluated in double, rounded once)
+ *   b_e = RN32(s_e + bias_e)              biased score, used only to choose
+ *   group score = RN32(top1 + top2) of the b_e in the group (the pages say the
+ *                 routing matches DeepSeek-V3, whose group score is the sum of
+ *                 the group's two best biased scores)
+ *   keep the topk_group best groups; among their experts take the topk best
+ *   b_e. Ties go to the lower index; the output is in descending b_e.
+ *   sum = RN32 running sum of the chosen s_e in output order
+ *   w_k = RN32(RN32(s_k / sum) * scale)
+ * ---------------------------------------------------------------------- */
+
+static float sigmoid_rn32(float z) { return (float)(1.0 / (1.0 + exp(-(double)z))); }
+
+/* index of the best of the first n values of v whose taken[] flag is 0
+ * (ties: the lower index); -1 if none */
+static int best_free(const float* v, const unsigned char* taken, int n) {
+    int best = -1;
+    for (int i = 0; i < n; ++i) {
+        if (taken[i]) continue;
+        if (best < 0 || v[i] > v[best]) best = i;
+    }
+    return best;
+}
+
+int oracle_route(const float* logits, const float* bias, int64_t T, int E, int n_group,
+                 int topk_group, int topk, float scale, int32_t* idx_out, float* w_out) {
+    if (E < 1 || n_group < 1 || E % n_group || topk_group < 1 || topk_group > n_group || topk < 1 ||
+        topk > (E / n_group) * topk_group || E > 4096 || topk > 64)
+        return -1;
+    const int gs = E / n_group;
+    float s[4096], b[4096], gscore[4096];
+    unsigned char taken[4096], gtaken[4096];
+    for (int64_t t = 0; t < T; ++t) {
+        const float* z = logits + t * E;
+        for (int e = 0; e < E; ++e) {
+            s[e] = sigmoid_rn32(z[e]);
+            b[e] = s[e] + bias[e];
+        }
+        /* group scores: sum of the group's two best biased scores */
+        for (int g = 0; g < n_group; ++g) {
+            memset(taken, 0, (size_t)gs);
+            int i1 = best_free(b + g * gs, taken, gs);
+            float top = b[g * gs + i1];
+            if (gs > 1) {
+                taken[i1] = 1;
+                int i2 = best_free(b + g * gs, taken, gs);
+                top = top + b[g * gs + i2];
+            }
+            gscore[g] = top;
+        }
+        /* keep the topk_group best groups; experts outside them are not eligible */
+        memset(gtaken, 0, (size_t)n_group);
+        memset(taken, 1, (size_t)E);
+        for (int k = 0; k < topk_group; ++k) {
+            int g = best_free(gscore, gtaken, n_group);
+            gtaken[g] = 1;
+            memset(taken + g * gs, 0, (size_t)gs);
+        }
+        /* topk best biased scores among the eligible experts, in descending order */
+        float sum = 0.0f;
+        int32_t* id = idx_out + t * topk;
+        for (int k = 0; k < topk; ++k) {
+            int e = best_free(b, taken, E);
+            taken[e] = 1;
+            id[k] = e;
+            sum = (k == 0) ? s[e] : sum + s[e];
+        }
+        for (int k = 0; k < topk; ++k) {
+            float q = s[id[k]] / sum;
+            w_out[t * topk + k] = q * scale;
+        }
+    }
+    return 0;
+}
+
+/* the FP32 sigmoid the router uses, exposed for the pins */
+float oracle_sigmoid(float z) { return sigmoid_rn32(z); }

@@ -58,6 +58,17 @@ MUTANTS = [
      "for (int k = 0; k < K; ++k) acc = fmaf(", "for (int k = K - 1; k >= 0; --k) acc = fmaf("),
     ("MoE uses the first routing weight for every expert", "fmaf(w[k],", "fmaf(w[0],"),
     ("MoE expert row index dropped", "e[(int64_t)k * D + j]", "e[(int64_t)k + j]"),
+    ("routing group score from the best expert only", "                top = top + b[g * gs + i2];",
+     "                top = top + 0.0f * b[g * gs + i2];"),
+    ("routing chooses by the unbiased score", "            b[e] = s[e] + bias[e];", "            b[e] = s[e];"),
+    ("routing weights from the biased score", "        for (int k = 0; k < topk; ++k) {\n            float q = s[id[k]] / sum;",
+     "        for (int k = 0; k < topk; ++k) {\n            float q = b[id[k]] / sum;"),
+    ("routing ties to the higher index", "        if (best < 0 || v[i] > v[best]) best = i;",
+     "        if (best < 0 || v[i] >= v[best]) best = i;"),
+    ("routing weights not renormalised", "            float q = s[id[k]] / sum;", "            float q = s[id[k]];"),
+    ("routing scale not applied", "            w_out[t * topk + k] = q * scale;", "            w_out[t * topk + k] = q;"),
+    ("routing sigmoid of the wrong sign", "static float sigmoid_rn32(float z) { return (float)(1.0 / (1.0 + exp(-(double)z))); }",
+     "static float sigmoid_rn32(float z) { return (float)(1.0 / (1.0 + exp((double)z))); }"),
     ("long-double residual coefficient squared",
      "long double c1 = sqrtl((long double)(n - 1) / (long double)n);\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i",
      "long double c1 = (long double)(n - 1) / (long double)n;\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i"),

@@ -500,3 +500,87 @@ def test_generator_distributions():
     assert np.allclose(w.sum(1), 2.5, atol=1e-5) and (w > 0).all()
     m = synth.bernoulli(4, 7, 200000, 1e-3)
     assert 120 < m.sum() < 290
+
+
+# ------------------------------------------------------------------- routing
+
+def _sigmoid_exact_f32(z: float) -> np.float32:
+    getcontext().prec = 60
+    v = Decimal(1) / (Decimal(1) + (-Decimal(float(z))).exp())
+    return nearest_f32(Fraction(v))
+
+
+def test_router_sigmoid_is_the_correctly_rounded_fp32_value():
+    rng = np.random.default_rng(60)
+    zs = np.concatenate([rng.standard_normal(1500) * 3, rng.uniform(-30, 30, 500),
+                         [0.0, 1e-8, -1e-8, 17.0, -17.0, 88.0, -88.0]]).astype(np.float32)
+    for z in zs:
+        assert f32(oracle.sigmoid(float(z))) == _sigmoid_exact_f32(float(z)), z
+
+
+def _route_inputs(T, E, seed, bias_scale=0.1):
+    rng = np.random.default_rng(seed)
+    z = (rng.standard_normal((T, E)) * 2).astype(np.float32)
+    b = (rng.standard_normal(E) * bias_scale).astype(np.float32)
+    return z, b
+
+
+def _biased(z, b):
+    s = np.array([[oracle.sigmoid(float(v)) for v in row] for row in z], np.float32)
+    return s, (s + b).astype(np.float32)
+
+
+def _order(v, eligible):
+    """indices of the eligible entries by descending value, ties by lower index (numpy lexsort)"""
+    idx = np.nonzero(eligible)[0]
+    return idx[np.lexsort((idx, -v[idx].astype(np.float64)))]
+
+
+def test_routing_without_groups_is_a_plain_top_k_of_biased_scores():
+    z, b = _route_inputs(16, 64, 61)
+    idx, w = oracle.route(z, b, n_group=1, topk_group=1, topk=6, scale=1.0)
+    s, bb = _biased(z, b)
+    for t in range(z.shape[0]):
+        assert np.array_equal(idx[t], _order(bb[t], np.ones(64, bool))[:6])
+
+
+def test_group_limited_routing_matches_a_numpy_restatement():
+    z, b = _route_inputs(24, 256, 62)
+    idx, w = oracle.route(z, b)  # 8 groups of 32, keep 4, top 8, scale 2.5
+    s, bb = _biased(z, b)
+    for t in range(z.shape[0]):
+        g = bb[t].reshape(8, 32)
+        top2 = -np.sort(-g, axis=1)[:, :2]
+        gscore = (top2[:, 0] + top2[:, 1]).astype(np.float32)
+        kept = _order(gscore, np.ones(8, bool))[:4]
+        elig = np.zeros(256, bool)
+        for k in kept:
+            elig[32 * k:32 * k + 32] = True
+        want = _order(bb[t], elig)[:8]
+        assert np.array_equal(idx[t], want)
+        assert all(e // 32 in kept for e in idx[t])
+        # weights: unbiased scores, running FP32 sum in output order, (s / sum) * 2.5
+        sel = s[t, idx[t]]
+        tot = sel[0]
+        for v in sel[1:]:
+            tot = f32(tot + v)
+        assert np.array_equal(w[t], ((sel / tot).astype(np.float32) * f32(2.5)).astype(np.float32))
+        assert abs(float(w[t].astype(np.float64).sum()) - 2.5) < 1e-5
+
+
+def test_routing_hand_example_with_a_group_tie():
+    # E = 8, two groups of 4, z = 0 so every sigmoid is exactly 0.5
+    z = np.zeros((1, 8), np.float32)
+    b = np.array([0.125, 0.375, 0, 0, 0.25, 0.25, 0.25, 0], np.float32)
+    # biased 0.625 0.875 0.5 0.5 | 0.75 0.75 0.75 0.5: both group scores are 1.5 -> group 0
+    idx, w = oracle.route(z, b, n_group=2, topk_group=1, topk=2, scale=2.5)
+    assert idx.tolist() == [[1, 0]] and w.tolist() == [[1.25, 1.25]]
+    # both groups kept: 0.875 first, then the first of the three 0.75 (expert 4)
+    idx, w = oracle.route(z, b, n_group=2, topk_group=2, topk=2, scale=2.5)
+    assert idx.tolist() == [[1, 4]] and w.tolist() == [[1.25, 1.25]]
+    # the weights come from the unbiased scores: a larger bias does not raise them
+    idx, w = oracle.route(np.array([[0, 2, 0, 0, 0, 0, 0, 0]], np.float32),
+                          np.array([1, 0, 0, 0, 0, 0, 0, 0], np.float32), 1, 1, 2, 1.0)
+    s1 = oracle.sigmoid(2.0)
+    assert idx.tolist() == [[0, 1]]
+    assert w[0, 0] == f32(f32(0.5) / f32(0.5 + s1)) and w[0, 0] < w[0, 1]
