@@ -251,6 +251,30 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
     return {k: round(v, 2) for k, v in out.items()}
 
 
+def route_latency(snr, device, reps: int = 50) -> float:
+    """Group-limited top-8 routing of T = 16384 tokens (256 experts, 8 groups, keep 4),
+    microseconds per launch; reported beside the step, which it is not part of."""
+    import torch
+    import synth
+    z = (synth.normal(3, 8, T_TOKENS * 256) * 2.0).reshape(T_TOKENS, 256)
+    b = synth.normal(3, 9, 256) * 0.05
+    zt, bt = torch.from_numpy(z).to(device), torch.from_numpy(b).to(device)
+    idx = torch.empty((T_TOKENS, 8), dtype=torch.int32, device=device)
+    w = torch.empty((T_TOKENS, 8), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            snr.moe_route(zt, bt, idx=idx, w=w, stream=stream)
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            snr.moe_route(zt, bt, idx=idx, w=w, stream=stream)
+        e.record(stream)
+    torch.cuda.synchronize(device)
+    snr.sync_status(stream)
+    return round(a.elapsed_time(e) * 1e3 / reps, 2)
+
+
 def bench_ours(args, rank, world, local_rank):
     import torch
     import sandwich_norm_residual_gb300 as snr
@@ -386,6 +410,7 @@ def bench_ours(args, rank, world, local_rank):
     }
     if not args.no_decode:
         line["config"]["decode"] = decode_latency(snr, device)
+        line["config"]["route_T16384_us"] = route_latency(snr, device)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)

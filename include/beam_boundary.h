@@ -125,6 +125,52 @@ BEAM_API beam_status beam_moe_combine_boundary(beam_stream_t stream, uint16_t* h
                                       float eps, int64_t T, int D, uint16_t* y_out);
 
 /*
+ * MoE boundary with the routing scale applied in the combine (SGLang page,
+ * "Dense layers and grouped MoE routing": the scale is applied while the
+ * experts are combined, or carried in the weights). topk_w are the
+ * renormalised routing weights without the scale;
+ *   x = bf16(RN32(route_scale * acc)),  acc as in beam_moe_combine_boundary.
+ * With route_scale = 1 this is beam_moe_combine_boundary. route_scale must be
+ * finite; other arguments and errors as beam_moe_combine_boundary.
+ */
+BEAM_API beam_status beam_moe_combine_boundary_scaled(beam_stream_t stream, uint16_t* h,
+                                             const uint16_t* expert_out, const float* topk_w,
+                                             float route_scale, const uint16_t* post_w,
+                                             const uint16_t* pre_w, int n, float eps, int64_t T,
+                                             int D, uint16_t* y_out);
+
+/* Router width and the largest top-k of beam_moe_route. */
+#define BEAM_ROUTE_EXPERTS 256
+#define BEAM_ROUTE_MAX_TOPK 16
+
+/*
+ * Group-limited top-k routing in front of the MoE combine (vLLM page, "MoE
+ * and residual stream": sigmoid scores plus a correction bias pick the best 4
+ * of 8 expert groups, then the top 8 experts, and the renormalised weights are
+ * scaled by 2.5; SGLang page, "Dense layers and grouped MoE routing": FP32
+ * logits and coefficients). Per token, FP32:
+ *   s_e = 1 / (1 + exp(-logit_e)),  b_e = s_e + bias_e
+ *   group score = sum of the group's two best b_e (the DeepSeek-V3 rule the
+ *   pages say Beam follows); keep the topk_group best of n_group groups;
+ *   take the topk best b_e among their experts, in descending order (ties to
+ *   the lower index);  topk_w[k] = (s_k / sum of the chosen s) * route_scale,
+ *   the sum taken in output order.
+ *   logits   [T, E] FP32 router logits, E = BEAM_ROUTE_EXPERTS; 16-byte aligned
+ *   bias     [E] FP32 correction bias; 16-byte aligned
+ *   n_group  1, 2, 4, 8, 16 or 32 (Beam: 8); topk_group in [1, n_group] (Beam: 4)
+ *   topk     in [1, BEAM_ROUTE_MAX_TOPK] and at most topk_group * E / n_group (Beam: 8)
+ *   topk_idx [T, topk] int32 expert ids, topk_w [T, topk] FP32; 4-byte aligned,
+ *            overlapping neither each other nor the inputs
+ * Logits must not be NaN (the choice among NaN scores is unspecified).
+ * exp is CUDA's FP32 expf, so s_e may differ from the correctly rounded
+ * sigmoid by a few ulps, and an exact tie between two biased scores may then
+ * break the other way.
+ */
+BEAM_API beam_status beam_moe_route(beam_stream_t stream, const float* logits, const float* bias,
+                                    int64_t T, int E, int n_group, int topk_group, int topk,
+                                    float route_scale, int32_t* topk_idx, float* topk_w);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. Returns BEAM_OK, BEAM_ERR_TIMEOUT if a kernel's bounded wait gave up
  * since the last read, or BEAM_ERR_CUDA if the synchronisation failed. The

@@ -74,6 +74,11 @@ def _load():
             lib.oracle_boundary_ld.restype = i32
             lib.oracle_residual_ld.argtypes = [vp, vp, i32, i64]
             lib.oracle_residual_ld.restype = None
+            lib.oracle_moe_combine_scaled.argtypes = [vp, vp, i32, i32, f32, vp]
+            lib.oracle_moe_combine_scaled.restype = None
+            lib.oracle_moe_boundary_scaled.argtypes = [vp, vp, vp, i32, f32, vp, vp, i32, f32, i64,
+                                                       i32, vp]
+            lib.oracle_moe_boundary_scaled.restype = i32
             lib.oracle_route.argtypes = [vp, vp, i64, i32, i32, i32, i32, f32, vp, vp]
             lib.oracle_route.restype = i32
             lib.oracle_sigmoid.argtypes = [f32]
@@ -171,8 +176,19 @@ def boundary(h, x, post_w, pre_w, n: int, eps: float, threads: int = 1):
     return h, y
 
 
-def moe_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: float, threads: int = 1):
-    """MoE combine + boundary; returns (h', y) as uint16 arrays [T, D]."""
+def moe_combine_scaled(e, w, scale: float) -> np.ndarray:
+    e = as_u16(e)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    K, D = e.shape
+    out = np.empty(D, np.uint16)
+    _load().oracle_moe_combine_scaled(_p(e), _p(w), K, D, scale, _p(out))
+    return out
+
+
+def moe_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: float, threads: int = 1,
+                 route_scale: float | None = None):
+    """MoE combine + boundary; returns (h', y) as uint16 arrays [T, D]. With route_scale the
+    scale is applied in the combine (x = bf16(scale * acc)) and topk_w are unscaled."""
     h = as_u16(h).copy()
     e = as_u16(expert_out)
     w = np.ascontiguousarray(topk_w.numpy() if hasattr(topk_w, "numpy") else topk_w,
@@ -184,8 +200,13 @@ def moe_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: float, threa
 
     def run(lo_hi):
         lo, hi = lo_hi
-        rc = lib.oracle_moe_boundary(_p(h[lo:hi]), _p(e[lo:hi]), _p(w[lo:hi]), K, _p(post_w),
-                                     _p(pre_w), n, eps, hi - lo, D, _p(y[lo:hi]))
+        if route_scale is None:
+            rc = lib.oracle_moe_boundary(_p(h[lo:hi]), _p(e[lo:hi]), _p(w[lo:hi]), K, _p(post_w),
+                                         _p(pre_w), n, eps, hi - lo, D, _p(y[lo:hi]))
+        else:
+            rc = lib.oracle_moe_boundary_scaled(_p(h[lo:hi]), _p(e[lo:hi]), _p(w[lo:hi]), K,
+                                                route_scale, _p(post_w), _p(pre_w), n, eps,
+                                                hi - lo, D, _p(y[lo:hi]))
         if rc != 0:
             raise ValueError("oracle_moe_boundary: bad arguments")
 

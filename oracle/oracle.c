@@ -195,13 +195,22 @@ void oracle_scales(int n, float* c1, float* c2) {
     *c2 = (float)(1.0 / sqrt((double)n));
 }
 
-/* x_j = bf16(fma chain over k of w_k * e_kj), e is [K, D], w is [K] */
-void oracle_moe_combine(const bf16_t* e, const float* w, int K, int D, bf16_t* x_out) {
+/* x_j = bf16(RN32(scale * fma chain over k of w_k * e_kj)), e is [K, D], w is [K].
+ * With the routing scale carried in w, scale is 1 and the product is exact. */
+static void moe_combine_scaled(const bf16_t* e, const float* w, int K, int D, float scale, bf16_t* x_out) {
     for (int j = 0; j < D; ++j) {
         float acc = 0.0f;
         for (int k = 0; k < K; ++k) acc = fmaf(w[k], oracle_bf16_to_f32(e[(int64_t)k * D + j]), acc);
-        x_out[j] = oracle_bf16_rne(acc);
+        x_out[j] = oracle_bf16_rne(scale * acc);
     }
+}
+
+void oracle_moe_combine(const bf16_t* e, const float* w, int K, int D, bf16_t* x_out) {
+    moe_combine_scaled(e, w, K, D, 1.0f, x_out);
+}
+
+void oracle_moe_combine_scaled(const bf16_t* e, const float* w, int K, int D, float scale, bf16_t* x_out) {
+    moe_combine_scaled(e, w, K, D, scale, x_out);
 }
 
 /* one row of the boundary given its (BF16) branch output x */
@@ -227,6 +236,23 @@ int oracle_boundary(bf16_t* h, const bf16_t* x, const bf16_t* post_w, const bf16
     for (int64_t t = 0; t < T; ++t)
         boundary_row(h + t * D, x + t * D, post_w, pre_w, c1, c2, eps, D, y + t * D, xn);
     free(xn);
+    return 0;
+}
+
+/* MoE boundary with the routing scale applied in the combine */
+int oracle_moe_boundary_scaled(bf16_t* h, const bf16_t* e, const float* topk_w, int K, float scale,
+                               const bf16_t* post_w, const bf16_t* pre_w, int n, float eps, int64_t T,
+                               int D, bf16_t* y) {
+    if (n < 1 || D < 1 || T < 0 || K < 1) return -1;
+    float c1, c2;
+    oracle_scales(n, &c1, &c2);
+    bf16_t* x = (bf16_t*)malloc(sizeof(bf16_t) * (size_t)D * 2);
+    if (!x) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        moe_combine_scaled(e + t * (int64_t)K * D, topk_w + t * K, K, D, scale, x);
+        boundary_row(h + t * D, x, post_w, pre_w, c1, c2, eps, D, y + t * D, x + D);
+    }
+    free(x);
     return 0;
 }
 

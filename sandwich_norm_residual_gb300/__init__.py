@@ -15,7 +15,7 @@ import ctypes
 from . import _lib
 from ._lib import LaunchOpts  # noqa: F401
 
-__all__ = ["boundary_fused", "moe_combine_boundary", "sync_status", "exact_sum_count",
+__all__ = ["boundary_fused", "moe_combine_boundary", "moe_route", "sync_status", "exact_sum_count",
            "version", "BeamError", "LaunchOpts", "library"]
 
 
@@ -84,10 +84,12 @@ def boundary_fused(h, x, post_w, pre_w, n: int, eps: float = 1e-6, y=None, strea
 
 
 def moe_combine_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: float = 1e-6, y=None,
-                         stream=None, opts=None):
+                         stream=None, opts=None, route_scale: float | None = None):
     """MoE boundary: combine the top-8 expert outputs with FP32 weights, then the dense boundary.
 
-    h: [T, D] bf16; expert_out: [T, 8, D] bf16; topk_w: [T, 8] float32 (routing scale included).
+    h: [T, D] bf16; expert_out: [T, 8, D] bf16; topk_w: [T, 8] float32 with the routing
+    scale included, or, when ``route_scale`` is given, without it (the kernel then applies
+    it to the combined sum).
     """
     import torch
     _check(h, "h", torch.bfloat16, 2)
@@ -105,6 +107,16 @@ def moe_combine_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: floa
         y = torch.empty_like(h)
     _check(y, "y", torch.bfloat16, 2)
     lib = _lib.load()
+    if route_scale is not None:
+        if opts is not None:
+            raise ValueError("route_scale and opts cannot be combined")
+        st = lib.beam_moe_combine_boundary_scaled(
+            _stream_ptr(stream), h.data_ptr(), expert_out.data_ptr(), topk_w.data_ptr(),
+            float(route_scale), post_w.data_ptr(), pre_w.data_ptr(), int(n), float(eps), T, D,
+            y.data_ptr())
+        if st != 0:
+            raise BeamError(st, "beam_moe_combine_boundary_scaled")
+        return y
     args = (_stream_ptr(stream), h.data_ptr(), expert_out.data_ptr(), topk_w.data_ptr(),
             post_w.data_ptr(), pre_w.data_ptr(), int(n), float(eps), T, D, y.data_ptr())
     st = lib.beam_moe_combine_boundary(*args) if opts is None else \
@@ -112,6 +124,33 @@ def moe_combine_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: floa
     if st != 0:
         raise BeamError(st, "beam_moe_combine_boundary")
     return y
+
+
+def moe_route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8,
+              route_scale: float = 2.5, idx=None, w=None, stream=None):
+    """Group-limited top-k routing on torch CUDA tensors.
+
+    logits: [T, 256] float32 router logits; bias: [256] float32 correction bias.
+    Returns (idx int32 [T, topk], w float32 [T, topk]).
+    """
+    import torch
+    _check(logits, "logits", torch.float32, 2)
+    _check(bias, "bias", torch.float32, 1)
+    T, E = logits.shape
+    if bias.shape[0] != E:
+        raise ValueError("bias must have one entry per expert")
+    if idx is None:
+        idx = torch.empty((T, topk), dtype=torch.int32, device=logits.device)
+    if w is None:
+        w = torch.empty((T, topk), dtype=torch.float32, device=logits.device)
+    _check(idx, "idx", torch.int32, 2)
+    _check(w, "w", torch.float32, 2)
+    st = _lib.load().beam_moe_route(_stream_ptr(stream), logits.data_ptr(), bias.data_ptr(), T, E,
+                                    int(n_group), int(topk_group), int(topk), float(route_scale),
+                                    idx.data_ptr(), w.data_ptr())
+    if st != 0:
+        raise BeamError(st, "beam_moe_route")
+    return idx, w
 
 
 def sync_status(stream=None) -> None:

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "boundary_kernels.cuh"
+#include "route.cuh"
 
 namespace {
 
@@ -239,7 +240,7 @@ beam_status check_common(int n, float eps, int64_t T, int D, const beam_launch_o
 
 beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* x, const uint16_t* e,
                    const float* w, const uint16_t* post_w, const uint16_t* pre_w, int n, float eps,
-                   int64_t T, int D, uint16_t* y, const beam_launch_opts* opts) {
+                   int64_t T, int D, uint16_t* y, const beam_launch_opts* opts, float route_scale = 1.0f) {
     DeviceInfo* info = nullptr;
     beam_status st = current_device(&info);
     if (st != BEAM_OK) return st;
@@ -325,6 +326,7 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
     p.stages = stages;
     p.wait_ns = kWaitNs;
     p.test_wait_ns = kTestWaitNs;
+    p.route_scale = route_scale;
 
     void* args[] = {&p};
     cudaError_t err;
@@ -379,12 +381,13 @@ beam_status beam_boundary_fused(beam_stream_t stream, uint16_t* h, const uint16_
     return beam_boundary_fused_ex(stream, h, x, post_w, pre_w, n, eps, T, D, y_out, nullptr);
 }
 
-beam_status beam_moe_combine_boundary_ex(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,
-                                         const float* topk_w, const uint16_t* post_w, const uint16_t* pre_w,
-                                         int n, float eps, int64_t T, int D, uint16_t* y_out,
-                                         const beam_launch_opts* opts) {
+static beam_status moe_boundary(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,
+                                const float* topk_w, float route_scale, const uint16_t* post_w,
+                                const uint16_t* pre_w, int n, float eps, int64_t T, int D, uint16_t* y_out,
+                                const beam_launch_opts* opts) {
     beam_status st = check_common(n, eps, T, D, opts);
     if (st != BEAM_OK || T == 0) return st;
+    if (!std::isfinite(route_scale)) return BEAM_ERR_ARG;
     if (!h || !expert_out || !topk_w || !post_w || !pre_w || !y_out) return BEAM_ERR_NULL;
     if (!aligned16(h) || !aligned16(expert_out) || !aligned16(topk_w) || !aligned16(post_w) ||
         !aligned16(pre_w) || !aligned16(y_out))
@@ -398,7 +401,59 @@ beam_status beam_moe_combine_boundary_ex(beam_stream_t stream, uint16_t* h, cons
     if (overlaps(h, rows, expert_out, erows) || overlaps(h, rows, topk_w, wbytes) || overlaps(h, rows, post_w, vec) ||
         overlaps(h, rows, pre_w, vec))
         return BEAM_ERR_ALIAS;
-    return launch(true, stream, h, nullptr, expert_out, topk_w, post_w, pre_w, n, eps, T, D, y_out, opts);
+    return launch(true, stream, h, nullptr, expert_out, topk_w, post_w, pre_w, n, eps, T, D, y_out, opts,
+                  route_scale);
+}
+
+beam_status beam_moe_combine_boundary_ex(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,
+                                         const float* topk_w, const uint16_t* post_w, const uint16_t* pre_w,
+                                         int n, float eps, int64_t T, int D, uint16_t* y_out,
+                                         const beam_launch_opts* opts) {
+    return moe_boundary(stream, h, expert_out, topk_w, 1.0f, post_w, pre_w, n, eps, T, D, y_out, opts);
+}
+
+beam_status beam_moe_combine_boundary_scaled(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,
+                                             const float* topk_w, float route_scale, const uint16_t* post_w,
+                                             const uint16_t* pre_w, int n, float eps, int64_t T, int D,
+                                             uint16_t* y_out) {
+    return moe_boundary(stream, h, expert_out, topk_w, route_scale, post_w, pre_w, n, eps, T, D, y_out,
+                        nullptr);
+}
+
+beam_status beam_moe_route(beam_stream_t stream, const float* logits, const float* bias, int64_t T, int E,
+                           int n_group, int topk_group, int topk, float route_scale, int32_t* topk_idx,
+                           float* topk_w) {
+    if (T < 0 || T > (int64_t(1) << 40) || E != BEAM_ROUTE_EXPERTS) return BEAM_ERR_SHAPE;
+    if (n_group < 1 || n_group > 32 || (n_group & (n_group - 1)) || topk_group < 1 || topk_group > n_group ||
+        topk < 1 || topk > BEAM_ROUTE_MAX_TOPK || topk > topk_group * (E / n_group) || !std::isfinite(route_scale))
+        return BEAM_ERR_ARG;
+    if (T == 0) return BEAM_OK;
+    if (!logits || !bias || !topk_idx || !topk_w) return BEAM_ERR_NULL;
+    if (!aligned16(logits) || !aligned16(bias) || (reinterpret_cast<uintptr_t>(topk_idx) & 3u) ||
+        (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+        return BEAM_ERR_ALIGN;
+    const size_t zb = (size_t)T * (size_t)E * 4u, ob = (size_t)T * (size_t)topk * 4u, bb = (size_t)E * 4u;
+    if (overlaps(topk_idx, ob, topk_w, ob) || overlaps(topk_idx, ob, logits, zb) || overlaps(topk_idx, ob, bias, bb) ||
+        overlaps(topk_w, ob, logits, zb) || overlaps(topk_w, ob, bias, bb))
+        return BEAM_ERR_ALIAS;
+    DeviceInfo* info = nullptr;
+    beam_status st = current_device(&info);
+    if (st != BEAM_OK) return st;
+    beam::RouteParams p;
+    p.logits = logits;
+    p.bias = bias;
+    p.idx = topk_idx;
+    p.w = topk_w;
+    p.T = T;
+    p.n_group = n_group;
+    p.topk_group = topk_group;
+    p.topk = topk;
+    p.scale = route_scale;
+    const int64_t blocks = (T + 7) / 8;  // 8 warps, one token each
+    if (blocks > 0x7FFFFFFF) return BEAM_ERR_SHAPE;
+    beam::route_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+    return BEAM_OK;
 }
 
 beam_status beam_moe_combine_boundary(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,

@@ -41,6 +41,7 @@ struct BoundaryParams {
     int stages;             // ring slots per CTA (ring kernel)
     unsigned long long wait_ns;       // bound of every mbarrier wait
     unsigned long long test_wait_ns;  // bound of the test hook's wait
+    float route_scale;      // MoE: x = bf16(route_scale * acc); 1 when the weights carry it
 };
 
 constexpr unsigned kFlagForceExact = 1u;
@@ -363,10 +364,12 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
                     }
                 }
             }
+            // routing scale applied in the combine (exact when it is 1)
+            const float2 rs2 = make_float2(p.route_scale, p.route_scale);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) set_word(xv[i], q, f2_to_bf2(acc[i][q]));
+                for (int q = 0; q < 4; ++q) set_word(xv[i], q, f2_to_bf2(__fmul2_rn(acc[i][q], rs2)));
         } else {
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {

@@ -160,3 +160,37 @@ def test_exact_count_rejects_null(lib):
 def test_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(ImportError, match="no CPU or PyTorch fallback"):
         _lib.load(str(tmp_path / "missing.so"))
+
+
+def test_route_and_scaled_combine_argument_errors(lib):
+    Z, Bi, I, W = A, A + (1 << 32), A + (2 << 32), A + (3 << 32)
+
+    def route(T=4, E=256, ng=8, tg=4, k=8, sc=2.5, z=Z, b=Bi, i=I, w=W):
+        return lib.beam_moe_route(None, z, b, T, E, ng, tg, k, sc, i, w)
+
+    assert route(E=128) == _lib.BEAM_ERR_SHAPE
+    assert route(T=-1) == _lib.BEAM_ERR_SHAPE
+    assert route(ng=6) == _lib.BEAM_ERR_ARG          # not a power of two
+    assert route(ng=64) == _lib.BEAM_ERR_ARG
+    assert route(tg=9) == _lib.BEAM_ERR_ARG
+    assert route(k=17) == _lib.BEAM_ERR_ARG
+    assert route(ng=32, tg=1, k=9) == _lib.BEAM_ERR_ARG  # one group of 8 experts
+    assert route(sc=float("inf")) == _lib.BEAM_ERR_ARG
+    assert route(T=0, z=None) == _lib.BEAM_OK
+    assert route(z=None) == _lib.BEAM_ERR_NULL
+    assert route(z=Z + 4) == _lib.BEAM_ERR_ALIGN
+    assert route(i=I + 2) == _lib.BEAM_ERR_ALIGN
+    assert route(w=I + 16) == _lib.BEAM_ERR_ALIAS    # weights over the ids
+    assert route(i=Z + 64) == _lib.BEAM_ERR_ALIAS    # ids inside the logits
+
+    def scaled(sc=2.5, **kw):
+        args = dict(h=A, e=A + (1 << 32), w=A + (5 << 32), pw=A + (2 << 32), qw=A + (3 << 32),
+                    y=A + (4 << 32))
+        args.update(kw)
+        return lib.beam_moe_combine_boundary_scaled(None, args["h"], args["e"], args["w"], sc,
+                                                    args["pw"], args["qw"], 2, 1e-6, 4, D,
+                                                    args["y"])
+
+    assert scaled(sc=float("nan")) == _lib.BEAM_ERR_ARG
+    assert scaled(e=None) == _lib.BEAM_ERR_NULL
+    assert scaled(y=A) == _lib.BEAM_ERR_ALIAS

@@ -584,3 +584,27 @@ def test_routing_hand_example_with_a_group_tie():
     s1 = oracle.sigmoid(2.0)
     assert idx.tolist() == [[0, 1]]
     assert w[0, 0] == f32(f32(0.5) / f32(0.5 + s1)) and w[0, 0] < w[0, 1]
+
+
+def test_scaled_combine_by_a_power_of_two_equals_prescaled_weights():
+    rng = np.random.default_rng(70)
+    e = bf16_bits(rng.standard_normal((8, 512)))
+    w = (rng.random(8) * 0.3).astype(np.float32)
+    for k in (-3, 1, 2):
+        sc = f32(2.0 ** k)
+        assert np.array_equal(oracle.moe_combine_scaled(e, w, float(sc)),
+                              oracle.moe_combine(e, (w * sc).astype(np.float32)))
+    assert np.array_equal(oracle.moe_combine_scaled(e, w, 1.0), oracle.moe_combine(e, w))
+
+
+def test_scaled_combine_rounds_the_scaled_fp32_sum_once():
+    rng = np.random.default_rng(71)
+    e = bf16_bits(rng.standard_normal((8, 96)))
+    w = (rng.random(8) * 0.3).astype(np.float32)
+    ef = bits_to_f32(e)
+    acc = [Fraction(0)] * 96
+    for k in range(8):
+        acc = [Fraction(float(nearest_f32(Fraction(float(w[k])) * Fraction(float(ef[k, j])) + acc[j])))
+               for j in range(96)]
+    want = bf16_bits([float(nearest_f32(Fraction(5, 2) * a)) for a in acc])
+    assert np.array_equal(oracle.moe_combine_scaled(e, w, 2.5), want)

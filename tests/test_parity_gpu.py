@@ -424,3 +424,64 @@ def test_pdl_on_the_prefill_and_moe_workloads():
     check(gpu_moe(m, 20, 1e-6, opts=opts), oracle_moe(m, 20, 1e-6), "moe pdl")
     check(gpu_dense(inp, cfg.n, cfg.eps, opts=dict(flags=snr._lib.BEAM_OPT_PDL, stages=2)),
           oracle_dense(inp, cfg.n, cfg.eps), "dense ring pdl")
+
+
+# --------------------------------------------------------------- routing and the scaled combine
+
+def _router_inputs(T, seed):
+    z = (synth.normal(seed, 8, T * 256) * 2.0).reshape(T, 256).astype(np.float32)
+    b = (synth.normal(seed, 9, 256) * 0.05).astype(np.float32)
+    return z, b
+
+
+def _check_routing(z, b, idx_g, w_g, idx_o, w_o, label):
+    """Exact selections on >= 99.99% of tokens; elsewhere the GPU's choice must be a near-tie
+    of the oracle's (the GPU's FP32 exp may differ by a few ulps). Weights of tokens with the
+    same selection agree to 16 ulps (2^-19 relative)."""
+    same = (idx_g == idx_o).all(1)
+    frac = float(same.mean())
+    s = np.array([[oracle.sigmoid(float(v)) for v in row] for row in z[~same]],
+                 np.float32).reshape(-1, z.shape[1])
+    bb = (s + b).astype(np.float64)
+    for r, (ig, io) in enumerate(zip(idx_g[~same], idx_o[~same])):
+        assert len(set(ig.tolist())) == len(ig)
+        assert np.all(np.abs(bb[r, ig] - bb[r, io]) <= 2.0 ** -19), (label, ig, io)
+    rel = np.abs(w_g[same].astype(np.float64) - w_o[same]) / np.abs(w_o[same])
+    print(f"{label}: identical selections {frac:.6f}, max weight error {rel.max():.3g} rel")
+    assert frac >= 0.9999 and rel.max() <= 2.0 ** -19
+
+
+@pytest.mark.parametrize("ng,tg,k,scale", [(8, 4, 8, 2.5), (1, 1, 8, 1.0), (32, 4, 6, 1.0),
+                                           (4, 2, 16, 2.5)])
+def test_routing_matches_the_oracle(ng, tg, k, scale):
+    T = 16384 if (ng, tg, k) == (8, 4, 8) else 1024
+    z, b = _router_inputs(T, 3)
+    idx_g, w_g = snr.moe_route(torch.from_numpy(z).to(DEV), torch.from_numpy(b).to(DEV), ng, tg, k,
+                               scale)
+    snr.sync_status()
+    idx_o, w_o = oracle.route(z, b, ng, tg, k, scale, threads=THREADS)
+    _check_routing(z, b, idx_g.cpu().numpy(), w_g.cpu().numpy(), idx_o, w_o,
+                   f"route ng={ng} tg={tg} k={k}")
+
+
+def test_routing_then_the_scaled_combine_boundary():
+    """route (weights without the scale) -> boundary with the scale applied in the combine;
+    and scale 1 reproduces the plain combine bit for bit."""
+    cfg = CONFIGS[3]
+    T = 512
+    z, b = _router_inputs(T, 5)
+    _, w = snr.moe_route(torch.from_numpy(z).to(DEV), torch.from_numpy(b).to(DEV), route_scale=1.0)
+    m = synth.moe_inputs(cfg, rows=T)
+    m["topk_w"] = w.cpu()
+    d = to_dev(m)
+    y = snr.moe_combine_boundary(d["h"], d["expert_out"], d["topk_w"], d["post_w"], d["pre_w"],
+                                 cfg.n, cfg.eps, route_scale=2.5)
+    snr.sync_status()
+    want = oracle.moe_boundary(m["h"], m["expert_out"], m["topk_w"], m["post_w"], m["pre_w"],
+                               cfg.n, cfg.eps, threads=THREADS, route_scale=2.5)
+    check((bits(d["h"]), bits(y)), want, "route + scaled combine")
+    d1 = to_dev(m)
+    y1 = snr.moe_combine_boundary(d1["h"], d1["expert_out"], d1["topk_w"], d1["post_w"],
+                                  d1["pre_w"], cfg.n, cfg.eps, route_scale=1.0)
+    plain = gpu_moe(m, cfg.n, cfg.eps)
+    assert np.array_equal(bits(d1["h"]), plain[0]) and np.array_equal(bits(y1), plain[1])
