@@ -79,6 +79,10 @@ def _load():
             lib.oracle_moe_boundary_scaled.argtypes = [vp, vp, vp, i32, f32, vp, vp, i32, f32, i64,
                                                        i32, vp]
             lib.oracle_moe_boundary_scaled.restype = i32
+            lib.oracle_ssmax_scale.argtypes = [i64]
+            lib.oracle_ssmax_scale.restype = f32
+            lib.oracle_qk_norm.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32]
+            lib.oracle_qk_norm.restype = i32
             lib.oracle_route.argtypes = [vp, vp, i64, i32, i32, i32, i32, f32, vp, vp]
             lib.oracle_route.restype = i32
             lib.oracle_sigmoid.argtypes = [f32]
@@ -269,3 +273,34 @@ def route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8,
 
     _run_rows(run, T, threads)
     return idx, w
+
+
+def ssmax_scale(pos: int) -> float:
+    return float(_load().oracle_ssmax_scale(int(pos)))
+
+
+def qk_norm(q, k, q_w, k_w, pos, table, eps: float, mode: str = "rope", threads: int = 1):
+    """Per-head Q/K RMSNorm then RoPE (mode "rope", FP32 cos/sin table [max_pos, 128]) or
+    SSMax on the queries (mode "ssmax"); returns new (q, k) uint16 arrays."""
+    q = as_u16(q).copy()
+    k = as_u16(k).copy()
+    q_w, k_w = as_u16(q_w), as_u16(k_w)
+    pos = np.ascontiguousarray(pos.numpy() if hasattr(pos, "numpy") else pos, dtype=np.int32)
+    T, nq, _ = q.shape
+    nk = k.shape[1]
+    if table is None:
+        table = np.zeros((1, 128), np.float32)
+    table = np.ascontiguousarray(table.numpy() if hasattr(table, "numpy") else table,
+                                 dtype=np.float32)
+    m = {"rope": 0, "ssmax": 1}[mode]
+    lib = _load()
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        rc = lib.oracle_qk_norm(_p(q[lo:hi]), _p(k[lo:hi]), _p(q_w), _p(k_w), _p(pos[lo:hi]),
+                                _p(table), table.shape[0], hi - lo, nq, nk, eps, m)
+        if rc != 0:
+            raise ValueError("oracle_qk_norm: bad arguments")
+
+    _run_rows(run, T, threads)
+    return q, k

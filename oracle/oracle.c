@@ -393,3 +393,64 @@ int oracle_route(const float* logits, const float* bias, int64_t T, int E, int n
 
 /* the FP32 sigmoid the router uses, exposed for the pins */
 float oracle_sigmoid(float z) { return sigmoid_rn32(z); }
+
+/* ------------------------------------------------------------------------
+ * Per-head Q/K RMSNorm with RoPE or SSMax (vLLM page, "Beam model
+ * architecture": Q and K are RMS-normalised per head before RoPE or SSMax;
+ * 48 query heads, 8 KV heads, head dimension 128; sliding-window layers use
+ * RoPE, full-attention layers use no positional encoding and scale each query
+ * by (1 + p/2048)^0.1 with p the 1-based position; HF page: the same scale
+ * written with the 0-based position, (1 + (pos+1)/2048)^0.1; FP32 at the norm,
+ * RoPE and query-scaling positions).
+ *
+ * Per head row v[0..127] (BF16), weight w:
+ *   vn_j = bf16((v_j * r) * w_j)  as oracle_rmsnorm (exact FP32 sum, one rounding)
+ * RoPE (rotate-half pairs j and j + 64, cos/sin from the caller's FP32 table
+ * row of the token's position: c_j = table[pos][j], s_j = table[pos][64 + j]):
+ *   out_j      = bf16(RN32(RN32(vn_j * c_j)      - RN32(vn_{j+64} * s_j)))
+ *   out_{j+64} = bf16(RN32(RN32(vn_{j+64} * c_j) + RN32(vn_j * s_j)))
+ * SSMax (queries only; keys keep vn):
+ *   g = RN32((1 + (pos + 1) / 2048)^0.1)   (evaluated in double, rounded once)
+ *   out_j = bf16(RN32(vn_j * g))
+ * ---------------------------------------------------------------------- */
+
+float oracle_ssmax_scale(int64_t pos) {
+    return (float)pow(1.0 + (double)(pos + 1) / 2048.0, 0.1);
+}
+
+static void rope_row(const bf16_t* vn, const float* cs, bf16_t* out) {
+    for (int j = 0; j < 64; ++j) {
+        float a = oracle_bf16_to_f32(vn[j]), b = oracle_bf16_to_f32(vn[j + 64]);
+        float c = cs[j], s = cs[64 + j];
+        float ac = a * c, bs = b * s, bc = b * c, as = a * s;
+        out[j] = oracle_bf16_rne(ac - bs);
+        out[j + 64] = oracle_bf16_rne(bc + as);
+    }
+}
+
+/* mode 0: RoPE on q and k; mode 1: SSMax on q, norm only on k.
+ * q [T, nq, 128] and k [T, nk, 128] are overwritten. Returns 0, or -1 on bad arguments. */
+int oracle_qk_norm(bf16_t* q, bf16_t* k, const bf16_t* qw, const bf16_t* kw, const int32_t* pos,
+                   const float* table, int64_t max_pos, int64_t T, int nq, int nk, float eps,
+                   int mode) {
+    if (T < 0 || nq < 0 || nk < 0 || (mode != 0 && mode != 1)) return -1;
+    bf16_t vn[128];
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t p = pos[t];
+        if (p < 0 || (mode == 0 && p >= max_pos)) return -1;
+        const float g = oracle_ssmax_scale(p);
+        for (int hh = 0; hh < nq + nk; ++hh) {
+            const int is_q = hh < nq;
+            bf16_t* row = is_q ? q + (t * nq + hh) * 128 : k + (t * nk + (hh - nq)) * 128;
+            oracle_rmsnorm(row, is_q ? qw : kw, eps, 128, vn);
+            if (mode == 0) {
+                rope_row(vn, table + p * 128, row);
+            } else if (is_q) {
+                for (int j = 0; j < 128; ++j) row[j] = oracle_bf16_rne(oracle_bf16_to_f32(vn[j]) * g);
+            } else {
+                memcpy(row, vn, sizeof vn);
+            }
+        }
+    }
+    return 0;
+}

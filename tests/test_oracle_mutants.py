@@ -69,6 +69,17 @@ MUTANTS = [
     ("routing scale not applied", "            w_out[t * topk + k] = q * scale;", "            w_out[t * topk + k] = q;"),
     ("routing sigmoid of the wrong sign", "static float sigmoid_rn32(float z) { return (float)(1.0 / (1.0 + exp(-(double)z))); }",
      "static float sigmoid_rn32(float z) { return (float)(1.0 / (1.0 + exp((double)z))); }"),
+    ("RoPE pairs neighbours instead of halves",
+     "float a = oracle_bf16_to_f32(vn[j]), b = oracle_bf16_to_f32(vn[j + 64]);",
+     "float a = oracle_bf16_to_f32(vn[j]), b = oracle_bf16_to_f32(vn[(j + 1) % 128]);"),
+    ("RoPE sine sign flipped", "out[j] = oracle_bf16_rne(ac - bs);", "out[j] = oracle_bf16_rne(ac + bs);"),
+    ("RoPE table row of the token index", "rope_row(vn, table + p * 128, row);",
+     "rope_row(vn, table + t * 128, row);"),
+    ("SSMax with the 0-based position", "return (float)pow(1.0 + (double)(pos + 1) / 2048.0, 0.1);",
+     "return (float)pow(1.0 + (double)pos / 2048.0, 0.1);"),
+    ("SSMax also scales keys", "            } else if (is_q) {", "            } else if (1) {"),
+    ("keys normalised with the query weight", "oracle_rmsnorm(row, is_q ? qw : kw, eps, 128, vn);",
+     "oracle_rmsnorm(row, qw, eps, 128, vn);"),
     ("long-double residual coefficient squared",
      "long double c1 = sqrtl((long double)(n - 1) / (long double)n);\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i",
      "long double c1 = (long double)(n - 1) / (long double)n;\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i"),

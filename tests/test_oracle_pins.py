@@ -608,3 +608,95 @@ def test_scaled_combine_rounds_the_scaled_fp32_sum_once():
                for j in range(96)]
     want = bf16_bits([float(nearest_f32(Fraction(5, 2) * a)) for a in acc])
     assert np.array_equal(oracle.moe_combine_scaled(e, w, 2.5), want)
+
+
+# ------------------------------------------------------------ Q/K norm, RoPE, SSMax
+
+def _qk_inputs(T, nq, nk, seed):
+    rng = np.random.default_rng(seed)
+    q = bf16_bits(rng.standard_normal((T, nq, 128)) * 3)
+    k = bf16_bits(rng.standard_normal((T, nk, 128)) * 3)
+    qw = bf16_bits(1 + 0.1 * rng.standard_normal(128))
+    kw = bf16_bits(1 + 0.1 * rng.standard_normal(128))
+    return q, k, qw, kw
+
+
+def _table(rows, c, s):
+    t = np.zeros((rows, 128), np.float32)
+    t[:, :64] = c
+    t[:, 64:] = s
+    return t
+
+
+def test_rope_identity_quarter_and_half_turn_rotations():
+    q, k, qw, kw = _qk_inputs(3, 4, 2, 80)
+    pos = np.array([0, 1, 2], np.int32)
+    tab = np.stack([_table(1, 1, 0)[0], _table(1, 0, 1)[0], _table(1, -1, 0)[0]])
+    qo, ko = oracle.qk_norm(q, k, qw, kw, pos, tab, 1e-6)
+    for t in range(3):
+        for h in range(4):
+            vn = oracle.rmsnorm(q[t, h], qw, 1e-6)
+            f = bits_to_f32(vn)
+            want = {0: f, 1: np.concatenate([-f[64:], f[:64]]), 2: -f}[t]
+            assert np.array_equal(bits_to_f32(qo[t, h]), want.astype(np.float32))
+        vk = bits_to_f32(oracle.rmsnorm(k[t, 1], kw, 1e-6))
+        assert np.array_equal(bits_to_f32(ko[t, 1]), {0: vk, 1: np.concatenate([-vk[64:], vk[:64]]),
+                                                      2: -vk}[t].astype(np.float32))
+
+
+def test_rope_matches_float32_rotation_steps_and_keeps_pair_norms():
+    q, k, qw, kw = _qk_inputs(4, 6, 2, 81)
+    rng = np.random.default_rng(82)
+    ang = rng.uniform(-np.pi, np.pi, (16, 64))
+    tab = np.concatenate([np.cos(ang), np.sin(ang)], 1).astype(np.float32)
+    pos = np.array([3, 9, 0, 15], np.int32)
+    qo, _ = oracle.qk_norm(q, k, qw, kw, pos, tab, 1e-6)
+    for t in range(4):
+        c, s = tab[pos[t], :64], tab[pos[t], 64:]
+        for h in range(6):
+            f = bits_to_f32(oracle.rmsnorm(q[t, h], qw, 1e-6))
+            a, b = f[:64], f[64:]
+            lo = bf16_bits((a * c) - (b * s))
+            hi = bf16_bits((b * c) + (a * s))
+            assert np.array_equal(qo[t, h], np.concatenate([lo, hi]))
+            o = bits_to_f32(qo[t, h]).astype(np.float64)
+            n_in = a.astype(np.float64) ** 2 + b.astype(np.float64) ** 2
+            n_out = o[:64] ** 2 + o[64:] ** 2
+            assert np.all(np.abs(n_out - n_in) <= 2.0 ** -6 * n_in + 1e-12)
+
+
+def test_rope_uses_the_row_of_each_tokens_position():
+    q, k, qw, kw = _qk_inputs(3, 2, 1, 83)
+    tab = _table(8, 1, 0)
+    tab[5] = _table(1, 0, 1)[0]          # a quarter turn only at position 5
+    qo, _ = oracle.qk_norm(q, k, qw, kw, np.array([4, 5, 6], np.int32), tab, 1e-6)
+    for t, turned in ((0, False), (1, True), (2, False)):
+        f = bits_to_f32(oracle.rmsnorm(q[t, 0], qw, 1e-6))
+        want = np.concatenate([-f[64:], f[:64]]) if turned else f
+        assert np.array_equal(bits_to_f32(qo[t, 0]), want.astype(np.float32))
+
+
+@pytest.mark.parametrize("p", [0, 1, 2047, 6143, 100000, 1048575])
+def test_ssmax_scale_is_the_rounded_power(p):
+    getcontext().prec = 60
+    x = Decimal(1) + Decimal(p + 1) / Decimal(2048)
+    exact = (Decimal("0.1") * x.ln()).exp()
+    assert f32(oracle.ssmax_scale(p)) == nearest_f32(Fraction(exact))
+    if p == 2047:
+        assert abs(oracle.ssmax_scale(p) - 2.0 ** 0.1) < 1e-7
+
+
+def test_ssmax_scales_queries_only_and_keys_keep_their_norm():
+    q, k, qw, kw = _qk_inputs(2, 3, 2, 84)
+    pos = np.array([10, 70000], np.int32)
+    qo, ko = oracle.qk_norm(q, k, qw, kw, pos, None, 1e-6, mode="ssmax")
+    for t in range(2):
+        g = f32(oracle.ssmax_scale(int(pos[t])))
+        for h in range(3):
+            f = bits_to_f32(oracle.rmsnorm(q[t, h], qw, 1e-6))
+            assert np.array_equal(qo[t, h], bf16_bits(f * g))
+        for h in range(2):
+            assert np.array_equal(ko[t, h], oracle.rmsnorm(k[t, h], kw, 1e-6))
+    # queries and keys use their own norm weights
+    qo2, ko2 = oracle.qk_norm(q, k, kw, qw, pos, None, 1e-6, mode="ssmax")
+    assert not np.array_equal(ko2, ko)
