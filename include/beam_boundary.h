@@ -170,11 +170,50 @@ BEAM_API beam_status beam_moe_route(beam_stream_t stream, const float* logits, c
                                     int64_t T, int E, int n_group, int topk_group, int topk,
                                     float route_scale, int32_t* topk_idx, float* topk_w);
 
+/* Head dimension and modes of beam_qk_norm. */
+#define BEAM_QK_HEAD_DIM 128
+#define BEAM_QK_ROPE 0
+#define BEAM_QK_SSMAX 1
+
+/*
+ * Per-head Q/K RMSNorm with RoPE or SSMax, in place (vLLM page, "Beam model
+ * architecture": Q and K are RMS-normalised per head before RoPE (sliding-
+ * window layers) or SSMax (full-attention layers, which scale each query by
+ * (1 + p/2048)^0.1, p the 1-based position); 48 query and 8 KV heads of 128).
+ * Per head row v, FP32 math:
+ *   vn = bf16((v * r) * w), r = 1/sqrt(RN32(exact sum of v^2)/128 + eps), w = q_w or k_w
+ *   BEAM_QK_ROPE:  rotate-half pairs (j, j+64) with c = rope_table[pos][j],
+ *     s = rope_table[pos][64 + j]: out_j = bf16(RN32(vn_j c) - RN32(vn_{j+64} s)),
+ *     out_{j+64} = bf16(RN32(vn_{j+64} c) + RN32(vn_j s)); queries and keys.
+ *   BEAM_QK_SSMAX: queries out = bf16(RN32(vn * g)),
+ *     g = RN32((1 + (pos + 1)/2048)^0.1) (pos 0-based, evaluated in double);
+ *     keys out = vn.
+ *   q [T, n_q_heads, 128], k [T, n_kv_heads, 128] BF16, overwritten; 16-byte aligned
+ *   q_w, k_w [128] BF16 norm weights; pos [T] int32 0-based positions
+ *   rope_table [max_pos, 128] FP32 (cos | sin), required for BEAM_QK_ROPE
+ *   head_dim must be BEAM_QK_HEAD_DIM; eps finite >= 0.
+ * A token whose position is negative, or not below max_pos with RoPE, is left
+ * untouched and beam_sync_status then returns BEAM_ERR_ARG.
+ */
+BEAM_API beam_status beam_qk_norm(beam_stream_t stream, uint16_t* q, uint16_t* k,
+                                  const uint16_t* q_w, const uint16_t* k_w, const int32_t* pos,
+                                  const float* rope_table, int64_t max_pos, int64_t T,
+                                  int n_q_heads, int n_kv_heads, int head_dim, float eps,
+                                  int mode);
+
+/* beam_qk_norm with BEAM_OPT_* flags (only BEAM_OPT_FORCE_EXACT_SUM applies). */
+BEAM_API beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k,
+                                     const uint16_t* q_w, const uint16_t* k_w, const int32_t* pos,
+                                     const float* rope_table, int64_t max_pos, int64_t T,
+                                     int n_q_heads, int n_kv_heads, int head_dim, float eps,
+                                     int mode, uint32_t flags);
+
 /*
  * Synchronises `stream`, then reads and clears the current device's status
- * word. Returns BEAM_OK, BEAM_ERR_TIMEOUT if a kernel's bounded wait gave up
- * since the last read, or BEAM_ERR_CUDA if the synchronisation failed. The
- * word is shared by all streams and threads using the device.
+ * word. Returns BEAM_OK; BEAM_ERR_TIMEOUT if a kernel's bounded wait gave up
+ * since the last read; BEAM_ERR_ARG if beam_qk_norm met a position out of
+ * range; or BEAM_ERR_CUDA if the synchronisation failed. The word is shared
+ * by all streams and threads using the device.
  */
 BEAM_API beam_status beam_sync_status(beam_stream_t stream);
 

@@ -15,7 +15,8 @@ import ctypes
 from . import _lib
 from ._lib import LaunchOpts  # noqa: F401
 
-__all__ = ["boundary_fused", "moe_combine_boundary", "moe_route", "sync_status", "exact_sum_count",
+__all__ = ["boundary_fused", "moe_combine_boundary", "moe_route", "qk_norm", "sync_status",
+           "exact_sum_count",
            "version", "BeamError", "LaunchOpts", "library"]
 
 
@@ -151,6 +152,36 @@ def moe_route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8
     if st != 0:
         raise BeamError(st, "beam_moe_route")
     return idx, w
+
+
+def qk_norm(q, k, q_w, k_w, pos, eps: float = 1e-6, mode: str = "rope", rope_table=None,
+            stream=None, force_exact: bool = False):
+    """Per-head Q/K RMSNorm then RoPE (mode "rope") or SSMax (mode "ssmax"), in place.
+
+    q: [T, n_q, 128] bf16; k: [T, n_kv, 128] bf16; q_w, k_w: [128] bf16; pos: [T] int32;
+    rope_table: [max_pos, 128] float32 (cos | sin), needed for mode "rope".
+    """
+    import torch
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k, "k", torch.bfloat16, 3)
+    _check(q_w, "q_w", torch.bfloat16, 1)
+    _check(k_w, "k_w", torch.bfloat16, 1)
+    _check(pos, "pos", torch.int32, 1)
+    T = q.shape[0]
+    if k.shape[0] != T or pos.shape[0] != T or q.shape[2] != k.shape[2]:
+        raise ValueError("shape mismatch: q [T, nq, 128], k [T, nk, 128], pos [T]")
+    m = {"rope": _lib.BEAM_QK_ROPE, "ssmax": _lib.BEAM_QK_SSMAX}[mode]
+    tab, max_pos = 0, 0
+    if mode == "rope":
+        _check(rope_table, "rope_table", torch.float32, 2)
+        tab, max_pos = rope_table.data_ptr(), rope_table.shape[0]
+    st = _lib.load().beam_qk_norm_ex(_stream_ptr(stream), q.data_ptr(), k.data_ptr(), q_w.data_ptr(),
+                                     k_w.data_ptr(), pos.data_ptr(), tab or None, max_pos, T,
+                                     q.shape[1], k.shape[1], q.shape[2], float(eps), m,
+                                     _lib.BEAM_OPT_FORCE_EXACT_SUM if force_exact else 0)
+    if st != 0:
+        raise BeamError(st, "beam_qk_norm")
+    return q, k
 
 
 def sync_status(stream=None) -> None:

@@ -21,6 +21,9 @@ BEAM_MAX_D = 32768
 BEAM_MOE_TOPK = 8
 BEAM_ROUTE_EXPERTS = 256
 BEAM_ROUTE_MAX_TOPK = 16
+BEAM_QK_HEAD_DIM = 128
+BEAM_QK_ROPE = 0
+BEAM_QK_SSMAX = 1
 BEAM_OPT_FORCE_EXACT_SUM = 0x1
 BEAM_OPT_TEST_WAIT_TIMEOUT = 0x2
 BEAM_OPT_PDL = 0x4
@@ -46,6 +49,10 @@ SIGNATURES = {
     "beam_moe_combine_boundary_scaled": (_i32, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _i32, _f32, _i64,
                                                  _i32, _vp]),
     "beam_moe_route": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
+    "beam_qk_norm": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _f32,
+                             _i32]),
+    "beam_qk_norm_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32,
+                                _f32, _i32, _u32]),
     "beam_sync_status": (_i32, [_vp]),
     "beam_exact_sum_count": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint64), _i32]),
     "beam_status_string": (ctypes.c_char_p, [_i32]),

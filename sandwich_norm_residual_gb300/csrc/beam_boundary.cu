@@ -14,6 +14,7 @@
 
 #include "boundary_kernels.cuh"
 #include "route.cuh"
+#include "qk_norm.cuh"
 
 namespace {
 
@@ -129,17 +130,17 @@ int choose_vpt(int nvec, bool moe) {
 // level (lane pair, 5 shuffle levels, nw-1 sequential block merges) adds
 // <= 2 (g + 1.01) u^2 T and raises the |c| bound g by 1.01 u T. The factor
 // 1.5 is slack; 1 + 2^-10 covers T <= s (1 + 2^-10).
-float error_factor(int vpt, int nt) {
+float error_factor_terms(double m, int levels) {
     const double u = std::ldexp(1.0, -24);
-    double m = 4.0 * vpt;
     double g = 1.01 * m, E = 0.505 * m * (m + 1.0);
-    int levels = 1 + 5 + (nt / 32 - 1);
     for (int i = 0; i < levels; ++i) {
         g += 1.01;
         E += 2.0 * g;
     }
     return (float)(E * u * u * 1.5 * (1.0 + 1.0 / 1024.0));
 }
+
+float error_factor(int vpt, int nt) { return error_factor_terms(4.0 * vpt, 1 + 5 + (nt / 32 - 1)); }
 
 beam_status current_device(DeviceInfo** info) {
     int dev = 0;
@@ -463,6 +464,61 @@ beam_status beam_moe_combine_boundary(beam_stream_t stream, uint16_t* h, const u
                                         nullptr);
 }
 
+beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k, const uint16_t* q_w,
+                            const uint16_t* k_w, const int32_t* pos, const float* rope_table, int64_t max_pos,
+                            int64_t T, int n_q_heads, int n_kv_heads, int head_dim, float eps, int mode,
+                            uint32_t flags) {
+    if (T < 0 || T > (int64_t(1) << 40) || head_dim != BEAM_QK_HEAD_DIM || n_q_heads < 0 || n_kv_heads < 0 ||
+        n_q_heads + n_kv_heads > 4096)
+        return BEAM_ERR_SHAPE;
+    if ((mode != BEAM_QK_ROPE && mode != BEAM_QK_SSMAX) || !(eps >= 0.0f) || !std::isfinite(eps) ||
+        (mode == BEAM_QK_ROPE && max_pos < 1) || (flags & ~BEAM_OPT_FORCE_EXACT_SUM))
+        return BEAM_ERR_ARG;
+    if (T == 0 || n_q_heads + n_kv_heads == 0) return BEAM_OK;
+    if ((n_q_heads && !q) || (n_kv_heads && !k) || !q_w || !k_w || !pos || (mode == BEAM_QK_ROPE && !rope_table))
+        return BEAM_ERR_NULL;
+    if ((q && !aligned16(q)) || (k && !aligned16(k)) || !aligned16(q_w) || !aligned16(k_w) ||
+        (reinterpret_cast<uintptr_t>(pos) & 3u) || (mode == BEAM_QK_ROPE && !aligned16(rope_table)))
+        return BEAM_ERR_ALIGN;
+    const size_t qb = (size_t)T * n_q_heads * head_dim * 2u, kb = (size_t)T * n_kv_heads * head_dim * 2u;
+    const size_t wb = (size_t)head_dim * 2u, pb = (size_t)T * 4u;
+    const size_t tb = mode == BEAM_QK_ROPE ? (size_t)max_pos * head_dim * 4u : 0u;
+    if (overlaps(q, qb, k, kb) || overlaps(q, qb, q_w, wb) || overlaps(q, qb, k_w, wb) || overlaps(q, qb, pos, pb) ||
+        overlaps(q, qb, rope_table, tb) || overlaps(k, kb, q_w, wb) || overlaps(k, kb, k_w, wb) ||
+        overlaps(k, kb, pos, pb) || overlaps(k, kb, rope_table, tb))
+        return BEAM_ERR_ALIAS;
+    DeviceInfo* info = nullptr;
+    beam_status st = current_device(&info);
+    if (st != BEAM_OK) return st;
+    beam::QKParams p;
+    p.q = q;
+    p.k = k;
+    p.qw = q_w;
+    p.kw = k_w;
+    p.pos = pos;
+    p.table = rope_table;
+    p.max_pos = max_pos;
+    p.T = T;
+    p.nq = n_q_heads;
+    p.nk = n_kv_heads;
+    p.eps = eps;
+    p.errk = error_factor_terms(2.0, 1 + 5);  // 2 terms per FP32 lane, lane merge + 5 shuffle levels
+    p.mode = mode;
+    p.flags = (flags & BEAM_OPT_FORCE_EXACT_SUM) ? beam::kFlagForceExact : 0u;
+    const int64_t blocks = (T + 7) / 8;  // 8 warps, one token each
+    if (blocks > 0x7FFFFFFF) return BEAM_ERR_SHAPE;
+    beam::qk_norm_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+    return BEAM_OK;
+}
+
+beam_status beam_qk_norm(beam_stream_t stream, uint16_t* q, uint16_t* k, const uint16_t* q_w, const uint16_t* k_w,
+                         const int32_t* pos, const float* rope_table, int64_t max_pos, int64_t T, int n_q_heads,
+                         int n_kv_heads, int head_dim, float eps, int mode) {
+    return beam_qk_norm_ex(stream, q, k, q_w, k_w, pos, rope_table, max_pos, T, n_q_heads, n_kv_heads, head_dim,
+                           eps, mode, 0u);
+}
+
 beam_status beam_sync_status(beam_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) {
@@ -476,7 +532,9 @@ beam_status beam_sync_status(beam_stream_t stream) {
         cudaGetLastError();
         return BEAM_ERR_CUDA;
     }
-    return word ? BEAM_ERR_TIMEOUT : BEAM_OK;
+    if (word & 1u) return BEAM_ERR_TIMEOUT;
+    if (word & 2u) return BEAM_ERR_ARG;
+    return BEAM_OK;
 }
 
 beam_status beam_exact_sum_count(beam_stream_t stream, uint64_t* count, int reset) {

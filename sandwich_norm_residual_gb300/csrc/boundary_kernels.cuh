@@ -127,7 +127,7 @@ __device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float e
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float2 f = bf2_to_f2(word(v[i], q));
-            two_sum_acc2(s, c, __fmul2_rn(f, f));
+            two_sum_acc2(s, c, mul2_rn(f, f));
         }
     float S = s.x, C = c.x;
     ff_merge(S, C, s.y, c.y);
@@ -237,7 +237,7 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
         for (int i = 0; i < VPT; ++i)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                set_word(hv[i], q, f2_to_bf2(__fmul2_rn(c1, bf2_to_f2(word(hv[i], q)))));
+                set_word(hv[i], q, f2_to_bf2(mul2_rn(c1, bf2_to_f2(word(hv[i], q)))));
     };
     float S1;
     const bool ok1 = block_sum_squares<VPT>(xv, p.errk, rs, &S1, scale_stream);
@@ -270,8 +270,8 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float2 xf = bf2_to_f2(word(xv[i], q));
-                float2 xn = bf2_to_f2(f2_to_bf2(__fmul2_rn(__fmul2_rn(xf, r1v), pw[q])));
-                uint32_t b = f2_to_bf2(__fmul2_rn(c2, xn));
+                float2 xn = bf2_to_f2(f2_to_bf2(mul2_rn(mul2_rn(xf, r1v), pw[q])));
+                uint32_t b = f2_to_bf2(mul2_rn(c2, xn));
                 set_word(hv[i], q, bf2_add(word(hv[i], q), b));
             }
         } else {
@@ -305,7 +305,7 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
             uint4 yv;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                set_word(yv, q, f2_to_bf2(__fmul2_rn(__fmul2_rn(bf2_to_f2(word(hv[i], q)), r2v), qw[q])));
+                set_word(yv, q, f2_to_bf2(mul2_rn(mul2_rn(bf2_to_f2(word(hv[i], q)), r2v), qw[q])));
             st_stream(p.y + base + (size_t)vi * 8, yv);
         }
     }
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) set_word(xv[i], q, f2_to_bf2(__fmul2_rn(acc[i][q], rs2)));
+                for (int q = 0; q < 4; ++q) set_word(xv[i], q, f2_to_bf2(mul2_rn(acc[i][q], rs2)));
         } else {
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {

@@ -41,17 +41,33 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
     return d;
 }
 
-__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+// Packed FP32 pairs in hand-written PTX with explicit .rn rounding: an
+// explicit rounding modifier keeps a multiply and a following add as two
+// roundings (PTX never contracts them into a fused multiply-add), which the
+// method's separately rounded FP32 products need.
+#define BEAM_F32X2_OP(NAME, OP)                                                                  \
+    __device__ __forceinline__ float2 NAME(float2 a, float2 b) {                                 \
+        float2 d;                                                                                \
+        asm("{\n\t.reg .b64 ra, rb, rd;\n\t"                                                    \
+            "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t" OP " rd, ra, rb;\n\t"          \
+            "mov.b64 {%0, %1}, rd;\n\t}"                                                          \
+            : "=f"(d.x), "=f"(d.y)                                                               \
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                          \
+        return d;                                                                                \
+    }
+BEAM_F32X2_OP(mul2_rn, "mul.rn.f32x2")
+BEAM_F32X2_OP(add2_rn, "add.rn.f32x2")
+BEAM_F32X2_OP(sub2_rn, "sub.rn.f32x2")
+#undef BEAM_F32X2_OP
 
 // s + c += t, error-free on (s, e) and accumulated into c, both lanes at once
-// (negation is an operand modifier of the packed add)
 __device__ __forceinline__ void two_sum_acc2(float2& s, float2& c, float2 t) {
-    float2 sn = __fadd2_rn(s, t);
-    float2 bp = __fadd2_rn(sn, neg2(s));
-    float2 ap = __fadd2_rn(sn, neg2(bp));
-    float2 db = __fadd2_rn(t, neg2(bp));
-    float2 da = __fadd2_rn(s, neg2(ap));
-    c = __fadd2_rn(c, __fadd2_rn(da, db));
+    float2 sn = add2_rn(s, t);
+    float2 bp = sub2_rn(sn, s);
+    float2 ap = sub2_rn(sn, bp);
+    float2 db = sub2_rn(t, bp);
+    float2 da = sub2_rn(s, ap);
+    c = add2_rn(c, add2_rn(da, db));
     s = sn;
 }
 

@@ -194,3 +194,24 @@ def test_route_and_scaled_combine_argument_errors(lib):
     assert scaled(sc=float("nan")) == _lib.BEAM_ERR_ARG
     assert scaled(e=None) == _lib.BEAM_ERR_NULL
     assert scaled(y=A) == _lib.BEAM_ERR_ALIAS
+
+
+def test_qk_norm_argument_errors(lib):
+    Q, K, QW, KW, P, TB = (A + (i << 32) for i in range(6))
+
+    def qk(T=4, nq=48, nk=8, hd=128, eps=1e-6, mode=0, max_pos=100, q=Q, k=K, qw=QW, kw=KW, p=P,
+           tb=TB):
+        return lib.beam_qk_norm(None, q, k, qw, kw, p, tb, max_pos, T, nq, nk, hd, eps, mode)
+
+    assert qk(hd=64) == _lib.BEAM_ERR_SHAPE
+    assert qk(T=-1) == _lib.BEAM_ERR_SHAPE
+    assert qk(mode=2) == _lib.BEAM_ERR_ARG
+    assert qk(eps=-1.0) == _lib.BEAM_ERR_ARG
+    assert qk(max_pos=0) == _lib.BEAM_ERR_ARG
+    assert qk(T=0, q=None) == _lib.BEAM_OK
+    assert qk(tb=None) == _lib.BEAM_ERR_NULL
+    assert qk(p=None) == _lib.BEAM_ERR_NULL
+    assert qk(q=Q + 8) == _lib.BEAM_ERR_ALIGN
+    assert qk(k=Q + 4 * 48 * 128 * 2 - 256) == _lib.BEAM_ERR_ALIAS
+    # SSMax needs no table
+    assert qk(mode=1, tb=None, max_pos=0) != _lib.BEAM_ERR_NULL

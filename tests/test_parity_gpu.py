@@ -485,3 +485,60 @@ def test_routing_then_the_scaled_combine_boundary():
                                   d1["pre_w"], cfg.n, cfg.eps, route_scale=1.0)
     plain = gpu_moe(m, cfg.n, cfg.eps)
     assert np.array_equal(bits(d1["h"]), plain[0]) and np.array_equal(bits(y1), plain[1])
+
+
+# --------------------------------------------------------------- per-head Q/K norm with RoPE / SSMax
+
+def _qk_case(T, nq, nk, seed, max_pos):
+    rng = np.random.default_rng(seed)
+    q = bf16(rng.standard_normal((T, nq, 128)) * 2)
+    k = bf16(rng.standard_normal((T, nk, 128)) * 2)
+    qw = bf16(1 + 0.1 * rng.standard_normal(128))
+    kw = bf16(1 + 0.1 * rng.standard_normal(128))
+    pos = torch.from_numpy(rng.integers(0, max_pos, T).astype(np.int32))
+    inv = 10000.0 ** (-np.arange(0, 128, 2) / 128.0)
+    ang = np.arange(max_pos)[:, None] * inv[None, :]
+    table = torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], 1).astype(np.float32))
+    return q, k, qw, kw, pos, table
+
+
+@pytest.mark.parametrize("mode", ["rope", "ssmax"])
+@pytest.mark.parametrize("T,nq,nk", [(16384, 48, 8), (5, 3, 1), (33, 48, 8), (7, 0, 8), (2, 48, 0)])
+def test_qk_norm_matches_the_oracle(mode, T, nq, nk):
+    max_pos = 4096 if mode == "rope" else 1 << 20
+    q, k, qw, kw, pos, table = _qk_case(T, nq, nk, T + nq, max_pos if mode == "rope" else 64)
+    if mode == "ssmax":
+        pos = torch.from_numpy(np.random.default_rng(T).integers(0, max_pos, T).astype(np.int32))
+    dq, dk = q.to(DEV), k.to(DEV)
+    snr.qk_norm(dq, dk, qw.to(DEV), kw.to(DEV), pos.to(DEV), 1e-6, mode,
+                rope_table=table.to(DEV) if mode == "rope" else None)
+    snr.sync_status()
+    wq, wk = oracle.qk_norm(q, k, qw, kw, pos, table if mode == "rope" else None, 1e-6, mode,
+                            threads=THREADS)
+    st_q = assert_parity(bits(dq), wq, f"qk {mode} q") if nq else None
+    st_k = assert_parity(bits(dk), wk, f"qk {mode} k") if nk else None
+    print(f"qk_norm {mode} T={T} nq={nq} nk={nk}: q {st_q} k {st_k}")
+
+
+def test_qk_norm_forced_exact_path_and_bad_positions():
+    q, k, qw, kw, pos, table = _qk_case(64, 48, 8, 90, 512)
+    a = (q.to(DEV), k.to(DEV))
+    snr.qk_norm(*a, qw.to(DEV), kw.to(DEV), pos.to(DEV), 1e-6, "rope", rope_table=table.to(DEV))
+    snr.exact_sum_count(reset=True)
+    b = (q.to(DEV), k.to(DEV))
+    snr.qk_norm(*b, qw.to(DEV), kw.to(DEV), pos.to(DEV), 1e-6, "rope", rope_table=table.to(DEV),
+                force_exact=True)
+    assert snr.exact_sum_count() == 64 * 56
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    # a token with a position outside the table is left as it was and reported
+    bad = pos.clone()
+    bad[3] = 512
+    c = (q.to(DEV), k.to(DEV))
+    snr.qk_norm(*c, qw.to(DEV), kw.to(DEV), bad.to(DEV), 1e-6, "rope", rope_table=table.to(DEV))
+    with pytest.raises(snr.BeamError) as ei:
+        snr.sync_status()
+    assert ei.value.status == snr._lib.BEAM_ERR_ARG
+    assert torch.equal(c[0][3].cpu(), q[3]) and torch.equal(c[1][3].cpu(), k[3])
+    keep = torch.arange(64) != 3
+    assert torch.equal(c[0][keep], a[0][keep])
+    snr.sync_status()  # cleared
