@@ -186,13 +186,14 @@ BEAM_API beam_status beam_moe_route(beam_stream_t stream, const float* logits, c
  *     s = rope_table[pos][64 + j]: out_j = bf16(RN32(vn_j c) - RN32(vn_{j+64} s)),
  *     out_{j+64} = bf16(RN32(vn_{j+64} c) + RN32(vn_j s)); queries and keys.
  *   BEAM_QK_SSMAX: queries out = bf16(RN32(vn * g)),
- *     g = RN32((1 + (pos + 1)/2048)^0.1) (pos 0-based, evaluated in double);
- *     keys out = vn.
+ *     g = RN32((1 + (pos + 1)/2048)^0.1) (pos 0-based, correctly rounded;
+ *     pos at most 2^24 - 2050); keys out = vn.
  *   q [T, n_q_heads, 128], k [T, n_kv_heads, 128] BF16, overwritten; 16-byte aligned
  *   q_w, k_w [128] BF16 norm weights; pos [T] int32 0-based positions
  *   rope_table [max_pos, 128] FP32 (cos | sin), required for BEAM_QK_ROPE
  *   head_dim must be BEAM_QK_HEAD_DIM; eps finite >= 0.
- * A token whose position is negative, or not below max_pos with RoPE, is left
+ * A token whose position is negative, not below max_pos (RoPE) or beyond the
+ * SSMax limit is left
  * untouched and beam_sync_status then returns BEAM_ERR_ARG.
  */
 BEAM_API beam_status beam_qk_norm(beam_stream_t stream, uint16_t* q, uint16_t* k,

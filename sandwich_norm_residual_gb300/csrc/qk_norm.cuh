@@ -9,10 +9,12 @@
 //          out_{j+64} = bf16(RN32(vn_{j+64} c_j) + RN32(vn_j s_j)),
 //          c_j = table[pos][j], s_j = table[pos][64 + j]   (rotate-half pairs)
 //   SSMax: out_j = bf16(RN32(vn_j g)), g = RN32((1 + (pos+1)/2048)^0.1) for
-//          queries (evaluated in double); keys keep vn.
+//          queries (correctly rounded, see ssmax_scale); keys keep vn.
 //
-// One warp per token walks its heads, 8 rows at a time. Lane l holds
-// elements 4l .. 4l+3 of a row, so the RoPE partner of lane l is lane l ^ 16.
+// One warp per token walks its heads: each pass takes 4 heads, one per group
+// of 8 lanes, and lane i of a group holds elements 16i .. 16i+15 of its head,
+// so the RoPE partner of a lane is lane ^ 4 and the row sums merge over 3
+// shuffle levels. Two batches of 8 heads are in flight at a time.
 #pragma once
 
 #include "row_sum.cuh"
@@ -21,7 +23,7 @@
 namespace beam {
 
 constexpr int kQKHeadDim = 128;
-constexpr int kQKBatch = 8;
+constexpr int kQKBatch = 8;           // heads per batch (two passes of 4)
 
 struct QKParams {
     uint16_t* q;          // [T, nq, 128] in/out
@@ -39,18 +41,21 @@ struct QKParams {
     unsigned flags;       // kFlagForceExact
 };
 
-// Exact RN32 sum of the squares of a 128-element row held as 4 values per
-// lane, for one warp (no shared memory): 32-bit chunk sums of each FP32 term
-// m * 2^q * 2^-149 in nine 64-bit registers, added across the warp, carried
-// and rounded to nearest even.
-__device__ __noinline__ float exact_warp_sum_squares(float v0, float v1, float v2, float v3) {
+// Exact RN32 sum of the squares of a 128-element row held by a group of 8
+// lanes (16 BF16 values per lane in a, b), without shared memory: 32-bit
+// chunk sums of each FP32 term m * 2^q * 2^-149 in nine 64-bit registers,
+// added over the group (xor 1, 2, 4), carried and rounded to nearest even.
+// Every lane of the warp must call it; each group gets its own row's sum.
+__device__ __noinline__ float exact_group_sum_squares(uint4 a, uint4 b) {
     unsigned long long acc[9];
 #pragma unroll
     for (int L = 0; L < 9; ++L) acc[L] = 0ull;
     int nan = 0, inf = 0;
-    const float v[4] = {v0, v1, v2, v3};
-    for (int i = 0; i < 4; ++i) {
-        const float t = __fmul_rn(v[i], v[i]);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t bits = (i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16);
+        const float x = __uint_as_float(bits);
+        const float t = __fmul_rn(x, x);
         const uint32_t u = __float_as_uint(t);
         const uint32_t E = (u >> 23) & 0xFFu, f = u & 0x7FFFFFu;
         if (E == 0xFFu) {
@@ -59,8 +64,8 @@ __device__ __noinline__ float exact_warp_sum_squares(float v0, float v1, float v
         }
         const uint32_t M = E ? (f | 0x800000u) : f;
         const uint32_t q = E ? E - 1u : 0u;
-        const unsigned long long w = (unsigned long long)M << (q & 31u);
-        const uint32_t k = q >> 5, lo = (uint32_t)w, hi = (uint32_t)(w >> 32);
+        const unsigned long long v = (unsigned long long)M << (q & 31u);
+        const uint32_t k = q >> 5, lo = (uint32_t)v, hi = (uint32_t)(v >> 32);
 #pragma unroll
         for (uint32_t L = 0; L < 9; ++L) {
             acc[L] += (L == k) ? lo : 0u;
@@ -69,11 +74,13 @@ __device__ __noinline__ float exact_warp_sum_squares(float v0, float v1, float v
     }
 #pragma unroll
     for (int L = 0; L < 9; ++L)
-        for (int off = 16; off; off >>= 1) acc[L] += __shfl_xor_sync(0xFFFFFFFFu, acc[L], off);
-    const int any_nan = __any_sync(0xFFFFFFFFu, nan), any_inf = __any_sync(0xFFFFFFFFu, inf);
-    if ((threadIdx.x & 31) == 0) atomicAdd(&g_exact_sum_count, 1ull);
-    if (any_nan) return __uint_as_float(0x7FFFFFFFu);
-    if (any_inf) return __uint_as_float(0x7F800000u);
+        for (int off = 4; off; off >>= 1) acc[L] += __shfl_xor_sync(0xFFFFFFFFu, acc[L], off);
+    for (int off = 4; off; off >>= 1) {
+        nan |= __shfl_xor_sync(0xFFFFFFFFu, nan, off);
+        inf |= __shfl_xor_sync(0xFFFFFFFFu, inf, off);
+    }
+    if (nan) return __uint_as_float(0x7FFFFFFFu);
+    if (inf) return __uint_as_float(0x7F800000u);
     uint32_t Lw[10];
     unsigned long long carry = 0ull;
     for (int L = 0; L < 10; ++L) {
@@ -84,91 +91,149 @@ __device__ __noinline__ float exact_warp_sum_squares(float v0, float v1, float v
     return limbs_to_f32(Lw);
 }
 
-__global__ void __launch_bounds__(256) qk_norm_kernel(const QKParams p) {
-    const int lane = threadIdx.x & 31;
+// Largest SSMax position: u = (2049 + pos) / 2048 is then exact in FP32.
+constexpr long long kSSMaxMaxPos = (1ll << 24) - 2050;
+
+// g = RN32(u^0.1), u = (2049 + pos)/2048, without a double pow (the FP64 pipe
+// is narrow). An FP32 estimate 2^(0.1 log2 u) is within a few ulps; lanes
+// 0..15 each take the candidate est + (lane - 8) ulps and test whether the
+// 10th power of its lower midpoint (exact in double, four double products,
+// relative error ~4e-16) is <= u. The 10th power is increasing, so the
+// correctly rounded g is the largest candidate that passes (no midpoint's
+// 10th power equals u for these positions: u^0.1 is irrational).
+// Called by the whole warp.
+__device__ __forceinline__ float ssmax_scale(long long pos, int lane) {
+    const float u = __fdiv_rn((float)(2049 + pos), 2048.0f);
+    const float est = exp2f(__fmul_rn(0.1f, log2f(u)));
+    bool below = false;
+    if (lane < 16) {
+        const uint32_t b = __float_as_uint(est) + (uint32_t)(lane - 8);
+        const double mid = 0.5 * ((double)__uint_as_float(b) + (double)__uint_as_float(b - 1u));
+        const double m2 = __dmul_rn(mid, mid), m4 = __dmul_rn(m2, m2), m8 = __dmul_rn(m4, m4);
+        below = __dmul_rn(m8, m2) <= (double)u;
+    }
+    const unsigned mask = __ballot_sync(0xFFFFFFFFu, below) & 0xFFFFu;
+    return __uint_as_float(__float_as_uint(est) + (uint32_t)((31 - __clz(mask)) - 8));
+}
+
+__global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
+    const int lane = threadIdx.x & 31, grp = lane >> 3, li = lane & 7;
     const long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= p.T) return;  // whole warps leave together
     const unsigned full = 0xFFFFFFFFu;
     const bool force_exact = (p.flags & kFlagForceExact) != 0;
 
     const long long pos = p.pos[t];
-    if (pos < 0 || (p.mode == 0 && pos >= p.max_pos)) {
+    if (pos < 0 || (p.mode == 0 && pos >= p.max_pos) || (p.mode != 0 && pos > kSSMaxMaxPos)) {
         if (lane == 0) atomicOr(&g_status_word, 2u);  // reported as a bad argument
         return;
     }
-    // per-lane constants: weights, and cos/sin (RoPE) or the query scale (SSMax)
-    const uint2 qwv = __ldg(reinterpret_cast<const uint2*>(p.qw) + lane);
-    const uint2 kwv = __ldg(reinterpret_cast<const uint2*>(p.kw) + lane);
-    float c[4] = {0.f, 0.f, 0.f, 0.f}, s[4] = {0.f, 0.f, 0.f, 0.f}, g = 1.0f;
-    if (p.mode == 0) {
-        const float* row = p.table + pos * kQKHeadDim + 4 * (lane & 15);
-        const float4 cc = __ldg(reinterpret_cast<const float4*>(row));
-        const float4 ss = __ldg(reinterpret_cast<const float4*>(row + 64));
-        c[0] = cc.x; c[1] = cc.y; c[2] = cc.z; c[3] = cc.w;
-        s[0] = ss.x; s[1] = ss.y; s[2] = ss.z; s[3] = ss.w;
-    } else {
-        double gd = 0.0;
-        if (lane == 0) gd = pow(1.0 + (double)(pos + 1) / 2048.0, 0.1);
-        g = (float)__shfl_sync(full, gd, 0);
-    }
-    const bool upper = lane >= 16;  // holds elements j + 64 of the rotate-half pairs
     const int nh = p.nq + p.nk;
+    const bool upper = li >= 4;  // holds elements j + 64 of the rotate-half pairs
 
-    for (int h0 = 0; h0 < nh; h0 += kQKBatch) {
-        uint2 v[kQKBatch];
-        uint16_t* rowp[kQKBatch];
+    // ---- loads of one batch: pass b takes head h0 + 4b + grp
+    auto row_of = [&](int hh) -> uint16_t* {
+        return hh < p.nq ? p.q + ((size_t)t * p.nq + hh) * kQKHeadDim
+                         : p.k + ((size_t)t * p.nk + (hh - p.nq)) * kQKHeadDim;
+    };
+    auto load = [&](uint4 (&v)[2][2], int h0) {
 #pragma unroll
-        for (int b = 0; b < kQKBatch; ++b) {
-            const int hh = h0 + b;
-            rowp[b] = hh < p.nq ? p.q + ((size_t)t * p.nq + hh) * kQKHeadDim
-                                : p.k + ((size_t)t * p.nk + (hh - p.nq)) * kQKHeadDim;
-            v[b] = hh < nh ? *reinterpret_cast<const uint2*>(rowp[b] + 4 * lane) : make_uint2(0, 0);
+        for (int b = 0; b < 2; ++b) {
+            const int hh = h0 + 4 * b + grp;
+            if (hh < nh) {
+                const uint4* r = reinterpret_cast<const uint4*>(row_of(hh) + 16 * li);
+                v[b][0] = r[0];
+                v[b][1] = r[1];
+            } else {
+                v[b][0] = v[b][1] = make_uint4(0, 0, 0, 0);
+            }
         }
+    };
+    uint4 va[2][2], vb[2][2];
+    load(va, 0);
+
+    // ---- per-lane constants: weights and cos/sin (RoPE) or the query scale (SSMax)
+    const uint4* qwp = reinterpret_cast<const uint4*>(p.qw + 16 * li);
+    const uint4* kwp = reinterpret_cast<const uint4*>(p.kw + 16 * li);
+    const uint4 qw0 = __ldg(qwp), qw1 = __ldg(qwp + 1), kw0 = __ldg(kwp), kw1 = __ldg(kwp + 1);
+    // cos | sin of this lane's 16 pairs (RoPE), re-read per head from L1
+    const float4* cs = p.mode == 0
+        ? reinterpret_cast<const float4*>(p.table + pos * kQKHeadDim + 16 * (li & 3)) : nullptr;
+    const float g = p.mode != 0 ? ssmax_scale(pos, lane) : 1.0f;
+
+    auto process = [&](const uint4 (&v)[2][2], int h0) {
 #pragma unroll
-        for (int b = 0; b < kQKBatch; ++b) {
-            const int hh = h0 + b;
-            if (hh >= nh) break;
-            const bool is_q = hh < p.nq;
-            const float2 x01 = bf2_to_f2(v[b].x), x23 = bf2_to_f2(v[b].y);
-            // compensated sum of squares, both FP32 lanes, then the warp
+        for (int b = 0; b < 2; ++b) {
+            const int hh = h0 + 4 * b + grp;
+            const bool live = hh < nh, is_q = hh < p.nq;
+            const uint32_t w[8] = {v[b][0].x, v[b][0].y, v[b][0].z, v[b][0].w,
+                                   v[b][1].x, v[b][1].y, v[b][1].z, v[b][1].w};
+            // compensated sum of squares over the group's 128 values
             float2 sa = make_float2(0.f, 0.f), ca = make_float2(0.f, 0.f);
-            two_sum_acc2(sa, ca, mul2_rn(x01, x01));
-            two_sum_acc2(sa, ca, mul2_rn(x23, x23));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 x = bf2_to_f2(w[i]);
+                two_sum_acc2(sa, ca, mul2_rn(x, x));
+            }
             float S = sa.x, C = ca.x;
             ff_merge(S, C, sa.y, ca.y);
 #pragma unroll
-            for (int off = 16; off; off >>= 1) {
-                const float s2 = __shfl_xor_sync(full, S, off), c2 = __shfl_xor_sync(full, C, off);
-                ff_merge(S, C, s2, c2);
+            for (int off = 4; off; off >>= 1) {
+                const float so = __shfl_xor_sync(full, S, off), co = __shfl_xor_sync(full, C, off);
+                ff_merge(S, C, so, co);
             }
             float Sr;
-            if (!certify_round(S, C, p.errk, &Sr) || force_exact)  // warp-uniform
-                Sr = exact_warp_sum_squares(x01.x, x01.y, x23.x, x23.y);
+            const bool need = !certify_round(S, C, p.errk, &Sr) || force_exact;  // group-uniform
+            if (__any_sync(full, need)) {
+                const float Sx = exact_group_sum_squares(v[b][0], v[b][1]);
+                if (need) {
+                    Sr = Sx;
+                    if (li == 0 && live) atomicAdd(&g_exact_sum_count, 1ull);
+                }
+            }
             const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(Sr, 128.0f), p.eps)));
             const float2 rv = make_float2(r, r);
-            const uint2 wv = is_q ? qwv : kwv;
-            const uint32_t n01 = f2_to_bf2(mul2_rn(mul2_rn(x01, rv), bf2_to_f2(wv.x)));
-            const uint32_t n23 = f2_to_bf2(mul2_rn(mul2_rn(x23, rv), bf2_to_f2(wv.y)));
-            uint2 out;
+            const uint4 w0 = is_q ? qw0 : kw0, w1 = is_q ? qw1 : kw1;
+            const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            uint32_t n[8], o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) n[i] = f2_to_bf2(mul2_rn(mul2_rn(bf2_to_f2(w[i]), rv), bf2_to_f2(ww[i])));
             if (p.mode == 0) {
-                const uint32_t m01 = __shfl_xor_sync(full, n01, 16), m23 = __shfl_xor_sync(full, n23, 16);
-                const float2 a01 = bf2_to_f2(n01), a23 = bf2_to_f2(n23);
-                const float2 b01 = bf2_to_f2(m01), b23 = bf2_to_f2(m23);
-                const float2 c01 = make_float2(c[0], c[1]), c23 = make_float2(c[2], c[3]);
-                const float2 s01 = make_float2(s[0], s[1]), s23 = make_float2(s[2], s[3]);
-                const float2 p01 = mul2_rn(a01, c01), p23 = mul2_rn(a23, c23);
-                const float2 q01 = mul2_rn(b01, s01), q23 = mul2_rn(b23, s23);
-                out.x = f2_to_bf2(upper ? add2_rn(p01, q01) : sub2_rn(p01, q01));
-                out.y = f2_to_bf2(upper ? add2_rn(p23, q23) : sub2_rn(p23, q23));
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    const float4 cc = __ldg(cs + i / 2), ss = __ldg(cs + 16 + i / 2);
+                    const float2 ci[2] = {make_float2(cc.x, cc.y), make_float2(cc.z, cc.w)};
+                    const float2 si[2] = {make_float2(ss.x, ss.y), make_float2(ss.z, ss.w)};
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t m = __shfl_xor_sync(full, n[i + u], 4);
+                        const float2 pa = mul2_rn(bf2_to_f2(n[i + u]), ci[u]);
+                        const float2 pb = mul2_rn(bf2_to_f2(m), si[u]);
+                        o[i + u] = f2_to_bf2(upper ? add2_rn(pa, pb) : sub2_rn(pa, pb));
+                    }
+                }
             } else if (is_q) {
                 const float2 gv = make_float2(g, g);
-                out.x = f2_to_bf2(mul2_rn(bf2_to_f2(n01), gv));
-                out.y = f2_to_bf2(mul2_rn(bf2_to_f2(n23), gv));
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = f2_to_bf2(mul2_rn(bf2_to_f2(n[i]), gv));
             } else {
-                out = make_uint2(n01, n23);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = n[i];
             }
-            *reinterpret_cast<uint2*>(rowp[b] + 4 * lane) = out;
+            if (live) {
+                uint4* dst = reinterpret_cast<uint4*>(row_of(hh) + 16 * li);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
         }
+    };
+
+    for (int h0 = 0; h0 < nh; h0 += 2 * kQKBatch) {
+        if (h0 + kQKBatch < nh) load(vb, h0 + kQKBatch);
+        process(va, h0);
+        if (h0 + kQKBatch >= nh) break;
+        if (h0 + 2 * kQKBatch < nh) load(va, h0 + 2 * kQKBatch);
+        process(vb, h0 + kQKBatch);
     }
 }
 

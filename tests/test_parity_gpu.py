@@ -520,6 +520,24 @@ def test_qk_norm_matches_the_oracle(mode, T, nq, nk):
     print(f"qk_norm {mode} T={T} nq={nq} nk={nk}: q {st_q} k {st_k}")
 
 
+def test_ssmax_scale_at_every_position_below_a_million():
+    """End to end at all 2^20 positions: a query head of ones, norm weight 1 and eps 0
+    give out = bf16(g), which must equal the BF16 rounding of the oracle's scale (the
+    FP32 midpoint selection itself is checked exhaustively on the CPU in
+    test_ssmax_method.py; BF16 output shows only the top 8 bits of g)."""
+    T = 1 << 20
+    q = torch.ones((T, 1, 128), dtype=torch.bfloat16)
+    k = torch.ones((T, 0, 128), dtype=torch.bfloat16)
+    w = torch.ones(128, dtype=torch.bfloat16)
+    pos = torch.arange(T, dtype=torch.int32)
+    dq = q.to(DEV)
+    snr.qk_norm(dq, k.to(DEV), w.to(DEV), w.to(DEV), pos.to(DEV), 0.0, "ssmax")
+    snr.sync_status()
+    want = np.array([oracle.ssmax_scale(p) for p in range(T)], np.float32)
+    got = bits(dq[:, 0, 0]).astype(np.uint32) << 16
+    assert np.array_equal(got, bits(torch.from_numpy(want).to(torch.bfloat16)).astype(np.uint32) << 16)
+
+
 def test_qk_norm_forced_exact_path_and_bad_positions():
     q, k, qw, kw, pos, table = _qk_case(64, 48, 8, 90, 512)
     a = (q.to(DEV), k.to(DEV))
