@@ -83,6 +83,19 @@ def _load():
             lib.oracle_ssmax_scale.restype = f32
             lib.oracle_qk_norm.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32]
             lib.oracle_qk_norm.restype = i32
+            u8 = ctypes.c_uint8
+            for name, res, args in (("oracle_e4m3", u8, [f32]), ("oracle_e2m1", u8, [f32]),
+                                    ("oracle_e4m3_to_f32", f32, [u8]),
+                                    ("oracle_e2m1_to_f32", f32, [u8])):
+                getattr(lib, name).argtypes = args
+                getattr(lib, name).restype = res
+            lib.oracle_nvfp4_row.argtypes = [vp, i32, f32, vp, vp]
+            lib.oracle_nvfp4_row.restype = None
+            lib.oracle_boundary_nvfp4.argtypes = [vp, vp, vp, vp, i32, f32, i64, i32, f32, vp, vp]
+            lib.oracle_boundary_nvfp4.restype = i32
+            lib.oracle_moe_boundary_nvfp4.argtypes = [vp, vp, vp, i32, vp, vp, i32, f32, i64, i32,
+                                                      f32, vp, vp]
+            lib.oracle_moe_boundary_nvfp4.restype = i32
             lib.oracle_route.argtypes = [vp, vp, i64, i32, i32, i32, i32, f32, vp, vp]
             lib.oracle_route.restype = i32
             lib.oracle_sigmoid.argtypes = [f32]
@@ -304,3 +317,74 @@ def qk_norm(q, k, q_w, k_w, pos, table, eps: float, mode: str = "rope", threads:
 
     _run_rows(run, T, threads)
     return q, k
+
+
+def e4m3(v: float) -> int:
+    return int(_load().oracle_e4m3(float(v)))
+
+
+def e2m1(v: float) -> int:
+    return int(_load().oracle_e2m1(float(v)))
+
+
+def e4m3_to_f32(b: int) -> float:
+    return float(_load().oracle_e4m3_to_f32(int(b)))
+
+
+def e2m1_to_f32(b: int) -> float:
+    return float(_load().oracle_e2m1_to_f32(int(b)))
+
+
+def nvfp4_row(y, gs: float):
+    """Quantise one BF16 row (length a multiple of 16): (q [D/2] uint8, sf [D/16] uint8)."""
+    y = as_u16(y)
+    D = y.size
+    q = np.empty(D // 2, np.uint8)
+    sf = np.empty(D // 16, np.uint8)
+    _load().oracle_nvfp4_row(_p(y), D, gs, _p(q), _p(sf))
+    return q, sf
+
+
+def boundary_nvfp4(h, x, post_w, pre_w, n: int, eps: float, gs: float, threads: int = 1):
+    """Dense boundary with y as NVFP4; returns (h', q [T, D/2], sf [T, D/16])."""
+    h = as_u16(h).copy()
+    x, post_w, pre_w = as_u16(x), as_u16(post_w), as_u16(pre_w)
+    T, D = h.shape
+    q = np.empty((T, D // 2), np.uint8)
+    sf = np.empty((T, D // 16), np.uint8)
+    lib = _load()
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        rc = lib.oracle_boundary_nvfp4(_p(h[lo:hi]), _p(x[lo:hi]), _p(post_w), _p(pre_w), n, eps,
+                                       hi - lo, D, gs, _p(q[lo:hi]), _p(sf[lo:hi]))
+        if rc != 0:
+            raise ValueError("oracle_boundary_nvfp4: bad arguments")
+
+    _run_rows(run, T, threads)
+    return h, q, sf
+
+
+def moe_boundary_nvfp4(h, expert_out, topk_w, post_w, pre_w, n: int, eps: float, gs: float,
+                       threads: int = 1):
+    """MoE boundary with y as NVFP4; returns (h', q [T, D/2], sf [T, D/16])."""
+    h = as_u16(h).copy()
+    e = as_u16(expert_out)
+    w = np.ascontiguousarray(topk_w.numpy() if hasattr(topk_w, "numpy") else topk_w,
+                             dtype=np.float32)
+    post_w, pre_w = as_u16(post_w), as_u16(pre_w)
+    T, K, D = e.shape
+    q = np.empty((T, D // 2), np.uint8)
+    sf = np.empty((T, D // 16), np.uint8)
+    lib = _load()
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        rc = lib.oracle_moe_boundary_nvfp4(_p(h[lo:hi]), _p(e[lo:hi]), _p(w[lo:hi]), K,
+                                           _p(post_w), _p(pre_w), n, eps, hi - lo, D, gs,
+                                           _p(q[lo:hi]), _p(sf[lo:hi]))
+        if rc != 0:
+            raise ValueError("oracle_moe_boundary_nvfp4: bad arguments")
+
+    _run_rows(run, T, threads)
+    return h, q, sf

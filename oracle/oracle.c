@@ -454,3 +454,119 @@ int oracle_qk_norm(bf16_t* q, bf16_t* k, const bf16_t* qw, const bf16_t* kw, con
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * NVFP4 output of the next pre-norm (SGLang page, "Fusion optimizations": the
+ * fusable boundary is extended to NVFP4). The pages give no format; this
+ * follows NVIDIA's published NVFP4 layout:
+ *   elements FP4 E2M1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit:
+ *   0, 0.5, 1, 1.5, 2, 3, 4, 6), two per byte, element 2i in the low nibble;
+ *   one FP8 E4M3 (OCP E4M3FN, bias 7, largest 448) scale per 16 consecutive
+ *   elements; an FP32 global scale gs from the caller.
+ * Per block of the BF16 row y:
+ *   amax = max |y_j|
+ *   sf   = E4M3(RN32(RN32(amax / 6) * gs))           nearest, ties to even, saturating
+ *   q_j  = sf == 0 ? +0 : E2M1(RN32(RN32(y_j * gs) / sf))
+ * Both conversions are written out as a nearest search over the format's
+ * finite values (ties to the even code, magnitudes above the largest value
+ * saturate, the sign is kept).
+ * ---------------------------------------------------------------------- */
+
+static float e4m3_value(unsigned code) { /* finite codes 0..0x7E of the magnitude */
+    unsigned e = (code >> 3) & 0xF, m = code & 7;
+    return e ? ldexpf(1.0f + (float)m / 8.0f, (int)e - 7) : ldexpf((float)m / 8.0f, -6);
+}
+
+static float e2m1_value(unsigned code) {
+    unsigned e = (code >> 1) & 3, m = code & 1;
+    return e ? ldexpf(1.0f + (float)m / 2.0f, (int)e - 1) : (m ? 0.5f : 0.0f);
+}
+
+/* nearest code (magnitude) among n_codes values, ties to the even code; saturates */
+static unsigned nearest_code(float mag, float (*value)(unsigned), unsigned n_codes) {
+    unsigned best = 0;
+    double bd = fabs((double)mag - (double)value(0));
+    for (unsigned c = 1; c < n_codes; ++c) {
+        double d = fabs((double)mag - (double)value(c));
+        if (d < bd || (d == bd && (c & 1u) == 0 && (best & 1u))) { best = c; bd = d; }
+    }
+    return best;
+}
+
+uint8_t oracle_e4m3(float v) {
+    unsigned s = signbit(v) ? 0x80u : 0u;
+    return (uint8_t)(s | nearest_code(fabsf(v), e4m3_value, 0x7F));
+}
+
+uint8_t oracle_e2m1(float v) {
+    unsigned s = signbit(v) ? 0x8u : 0u;
+    return (uint8_t)(s | nearest_code(fabsf(v), e2m1_value, 8));
+}
+
+float oracle_e4m3_to_f32(uint8_t b) {
+    float m = e4m3_value(b & 0x7Fu);
+    return (b & 0x80u) ? -m : m;
+}
+
+float oracle_e2m1_to_f32(uint8_t b) {
+    float m = e2m1_value(b & 7u);
+    return (b & 8u) ? -m : m;
+}
+
+/* quantise a BF16 row of D (a multiple of 16) values: q [D/2] bytes, sf [D/16] bytes */
+void oracle_nvfp4_row(const bf16_t* y, int D, float gs, uint8_t* q, uint8_t* sf) {
+    for (int blk = 0; blk < D / 16; ++blk) {
+        float amax = 0.0f;
+        for (int j = 0; j < 16; ++j) {
+            float a = fabsf(oracle_bf16_to_f32(y[blk * 16 + j]));
+            if (a > amax) amax = a;
+        }
+        float t = amax / 6.0f;
+        uint8_t s = oracle_e4m3(t * gs);
+        float sv = oracle_e4m3_to_f32(s);
+        sf[blk] = s;
+        for (int j = 0; j < 16; j += 2) {
+            uint8_t lo = 0, hi = 0;
+            if (sv != 0.0f) {
+                float a = (oracle_bf16_to_f32(y[blk * 16 + j]) * gs) / sv;
+                float b = (oracle_bf16_to_f32(y[blk * 16 + j + 1]) * gs) / sv;
+                lo = oracle_e2m1(a);
+                hi = oracle_e2m1(b);
+            }
+            q[(blk * 16 + j) / 2] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+/* dense boundary whose y leaves as NVFP4 */
+int oracle_boundary_nvfp4(bf16_t* h, const bf16_t* x, const bf16_t* post_w, const bf16_t* pre_w,
+                          int n, float eps, int64_t T, int D, float gs, uint8_t* q, uint8_t* sf) {
+    if (D % 16) return -1;
+    bf16_t* y = (bf16_t*)malloc(sizeof(bf16_t) * (size_t)D);
+    if (!y) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        if (oracle_boundary(h + t * D, x + t * D, post_w, pre_w, n, eps, 1, D, y) != 0) { free(y); return -1; }
+        oracle_nvfp4_row(y, D, gs, q + t * (D / 2), sf + t * (D / 16));
+    }
+    free(y);
+    return 0;
+}
+
+/* MoE boundary whose y leaves as NVFP4 */
+int oracle_moe_boundary_nvfp4(bf16_t* h, const bf16_t* e, const float* topk_w, int K,
+                              const bf16_t* post_w, const bf16_t* pre_w, int n, float eps, int64_t T,
+                              int D, float gs, uint8_t* q, uint8_t* sf) {
+    if (D % 16) return -1;
+    bf16_t* y = (bf16_t*)malloc(sizeof(bf16_t) * (size_t)D);
+    if (!y) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        if (oracle_moe_boundary(h + t * D, e + t * (int64_t)K * D, topk_w + t * K, K, post_w, pre_w, n, eps, 1,
+                                D, y) != 0) {
+            free(y);
+            return -1;
+        }
+        oracle_nvfp4_row(y, D, gs, q + t * (D / 2), sf + t * (D / 16));
+    }
+    free(y);
+    return 0;
+}

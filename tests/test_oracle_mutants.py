@@ -80,6 +80,15 @@ MUTANTS = [
     ("SSMax also scales keys", "            } else if (is_q) {", "            } else if (1) {"),
     ("keys normalised with the query weight", "oracle_rmsnorm(row, is_q ? qw : kw, eps, 128, vn);",
      "oracle_rmsnorm(row, qw, eps, 128, vn);"),
+    ("NVFP4 block max without the absolute value",
+     "float a = fabsf(oracle_bf16_to_f32(y[blk * 16 + j]));", "float a = oracle_bf16_to_f32(y[blk * 16 + j]);"),
+    ("NVFP4 scale without the E2M1 maximum", "float t = amax / 6.0f;", "float t = amax;"),
+    ("NVFP4 nibbles swapped", "q[(blk * 16 + j) / 2] = (uint8_t)(lo | (hi << 4));",
+     "q[(blk * 16 + j) / 2] = (uint8_t)(hi | (lo << 4));"),
+    ("FP8/FP4 ties away from zero", "if (d < bd || (d == bd && (c & 1u) == 0 && (best & 1u))) { best = c; bd = d; }",
+     "if (d < bd || (d == bd && c > best)) { best = c; bd = d; }"),
+    ("NVFP4 quantises with the global scale inverted", "float a = (oracle_bf16_to_f32(y[blk * 16 + j]) * gs) / sv;",
+     "float a = (oracle_bf16_to_f32(y[blk * 16 + j]) / gs) / sv;"),
     ("long-double residual coefficient squared",
      "long double c1 = sqrtl((long double)(n - 1) / (long double)n);\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i",
      "long double c1 = (long double)(n - 1) / (long double)n;\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i"),

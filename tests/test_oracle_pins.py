@@ -700,3 +700,58 @@ def test_ssmax_scales_queries_only_and_keys_keep_their_norm():
     # queries and keys use their own norm weights
     qo2, ko2 = oracle.qk_norm(q, k, kw, qw, pos, None, 1e-6, mode="ssmax")
     assert not np.array_equal(ko2, ko)
+
+
+# -------------------------------------------------------------------- NVFP4 output
+
+def test_e4m3_matches_torch_float8_cast_in_range():
+    rng = np.random.default_rng(90)
+    v = np.concatenate([rng.uniform(-448, 448, 4000), rng.standard_normal(4000) * 0.01,
+                        np.ldexp(rng.integers(1, 16, 500) * 0.5 + 0.25, rng.integers(-9, 8, 500))])
+    v = v.astype(np.float32)
+    v = v[np.abs(v) <= 448]  # torch's cast turns larger values into NaN; these saturate
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3(float(x)) for x in v], np.uint8)
+    assert np.array_equal(got, want)
+    assert oracle.e4m3_to_f32(oracle.e4m3(1e6)) == 448.0        # saturates
+    assert oracle.e4m3_to_f32(oracle.e4m3(-470.0)) == -448.0
+
+
+def test_e2m1_rounding_table():
+    # the eight magnitudes 0 0.5 1 1.5 2 3 4 6; halfway cases go to the even code
+    cases = {0.25: 0.0, 0.26: 0.5, 0.75: 1.0, 1.25: 1.0, 1.3: 1.5, 1.75: 2.0, 2.5: 2.0,
+             2.6: 3.0, 3.5: 4.0, 5.0: 4.0, 5.1: 6.0, 6.0: 6.0, 7.0: 6.0, 1e9: 6.0, -1.75: -2.0,
+             -5.0: -4.0, 0.0: 0.0}
+    for v, want in cases.items():
+        assert oracle.e2m1_to_f32(oracle.e2m1(v)) == want, v
+    assert oracle.e2m1(-0.1) == 0x8   # the sign is kept (-0)
+
+
+def test_nvfp4_hand_block():
+    # gs = 1, amax = 3: sf = e4m3(3/6) = 0.5, q = e2m1(2 y)
+    y = np.array([1, 2, 3, -1, 0.25, 0, -3, 0.5, 1.5, -2, 0.125, 0, 0, 0, 0, 0.75], np.float32)
+    q, sf = oracle.nvfp4_row(bf16_bits(y), 1.0)
+    assert oracle.e4m3_to_f32(int(sf[0])) == 0.5
+    nib = [int(q[i // 2]) >> (4 * (i % 2)) & 0xF for i in range(16)]
+    vals = [oracle.e2m1_to_f32(c) for c in nib]
+    assert vals == [2, 4, 6, -2, 0.5, 0, -6, 1, 3, -4, 0, 0, 0, 0, 0, 1.5]
+    # an all-zero block has scale 0 and zero codes
+    q, sf = oracle.nvfp4_row(np.zeros(16, np.uint16), 448.0)
+    assert sf[0] == 0 and not q.any()
+
+
+def test_nvfp4_dequantises_within_half_a_step():
+    rng = np.random.default_rng(91)
+    y = bf16_bits(rng.standard_normal(5120) * 2)
+    yf = bits_to_f32(y).astype(np.float64)
+    gs = 448.0 * 6.0 / float(np.abs(yf).max())
+    q, sf = oracle.nvfp4_row(y, gs)
+    for blk in range(5120 // 16):
+        s = oracle.e4m3_to_f32(int(sf[blk]))
+        seg = yf[blk * 16:(blk + 1) * 16]
+        codes = [int(q[(blk * 16 + i) // 2]) >> (4 * (i % 2)) & 0xF for i in range(16)]
+        deq = np.array([oracle.e2m1_to_f32(c) for c in codes]) * s / gs
+        amax = np.abs(seg).max()
+        # scale rounding (E4M3, 4 significant bits) may clip the top value a little; the
+        # grid step near amax is 2 (in scaled units) -> half a step is amax/6, plus clipping
+        assert np.all(np.abs(deq - seg) <= amax / 6 + 2 ** -4 * amax + 1e-12)
