@@ -272,6 +272,38 @@ BEAM_API beam_status beam_moe_combine_boundary_ex(beam_stream_t stream, uint16_t
                                          const beam_launch_opts* opts);
 
 /*
+ * The dense and MoE boundaries with y leaving as NVFP4 for the next GEMM
+ * (SGLang page, "Fusion optimizations": the fusable boundary is extended to
+ * NVFP4). The pages give no format; this is NVIDIA's published NVFP4 layout.
+ * y is computed as in the BF16 calls, then, per block of 16 consecutive values
+ * of a row:
+ *   amax = max |y|,  sf = E4M3(RN32(RN32(amax / 6) * y_global_scale))
+ *   q_j  = E2M1(RN32(y_j * RN32(y_global_scale / sf))), or 0 when sf is 0
+ * (E4M3 = OCP E4M3FN, largest 448; E2M1 values 0, 0.5, 1, 1.5, 2, 3, 4, 6;
+ * both nearest-even and saturating; signs kept).
+ *   y_fp4   [T, D/2] bytes: element 2i in the low nibble, 2i+1 in the high; 16-byte aligned
+ *   y_scale [T, D/16] bytes: one E4M3 scale per block, row-major (no swizzle)
+ *   y_global_scale finite > 0; D a multiple of 16; no BF16 y is written.
+ * Other arguments and errors as beam_boundary_fused_ex / beam_moe_combine_boundary_ex;
+ * opts may be NULL; options of the shared-memory ring (stages > 0, the wait
+ * timeout hook) give BEAM_ERR_ARG. y_fp4 and y_scale overlap neither each other
+ * nor any other operand.
+ * y must be finite for the codes to be defined.
+ */
+BEAM_API beam_status beam_boundary_fused_nvfp4(beam_stream_t stream, uint16_t* h, const uint16_t* x,
+                                      const uint16_t* post_w, const uint16_t* pre_w, int n,
+                                      float eps, int64_t T, int D, float y_global_scale,
+                                      uint8_t* y_fp4, uint8_t* y_scale,
+                                      const beam_launch_opts* opts);
+
+BEAM_API beam_status beam_moe_combine_boundary_nvfp4(beam_stream_t stream, uint16_t* h,
+                                            const uint16_t* expert_out, const float* topk_w,
+                                            const uint16_t* post_w, const uint16_t* pre_w, int n,
+                                            float eps, int64_t T, int D, float y_global_scale,
+                                            uint8_t* y_fp4, uint8_t* y_scale,
+                                            const beam_launch_opts* opts);
+
+/*
  * Synchronises `stream` and returns in *count the number of row sums (two per
  * row: the post-norm and the pre-norm sum) that took the exact integer path on
  * the current device since the last reset; reset != 0 zeroes the counter.

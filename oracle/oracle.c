@@ -466,7 +466,8 @@ int oracle_qk_norm(bf16_t* q, bf16_t* k, const bf16_t* qw, const bf16_t* kw, con
  * Per block of the BF16 row y:
  *   amax = max |y_j|
  *   sf   = E4M3(RN32(RN32(amax / 6) * gs))           nearest, ties to even, saturating
- *   q_j  = sf == 0 ? +0 : E2M1(RN32(RN32(y_j * gs) / sf))
+ *   inv  = RN32(gs / sf)                              one division per block
+ *   q_j  = sf == 0 ? +0 : E2M1(RN32(y_j * inv))
  * Both conversions are written out as a nearest search over the format's
  * finite values (ties to the even code, magnitudes above the largest value
  * saturate, the sign is kept).
@@ -525,11 +526,12 @@ void oracle_nvfp4_row(const bf16_t* y, int D, float gs, uint8_t* q, uint8_t* sf)
         uint8_t s = oracle_e4m3(t * gs);
         float sv = oracle_e4m3_to_f32(s);
         sf[blk] = s;
+        const float inv = sv != 0.0f ? gs / sv : 0.0f;
         for (int j = 0; j < 16; j += 2) {
             uint8_t lo = 0, hi = 0;
             if (sv != 0.0f) {
-                float a = (oracle_bf16_to_f32(y[blk * 16 + j]) * gs) / sv;
-                float b = (oracle_bf16_to_f32(y[blk * 16 + j + 1]) * gs) / sv;
+                float a = oracle_bf16_to_f32(y[blk * 16 + j]) * inv;
+                float b = oracle_bf16_to_f32(y[blk * 16 + j + 1]) * inv;
                 lo = oracle_e2m1(a);
                 hi = oracle_e2m1(b);
             }

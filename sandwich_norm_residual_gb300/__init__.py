@@ -15,7 +15,8 @@ import ctypes
 from . import _lib
 from ._lib import LaunchOpts  # noqa: F401
 
-__all__ = ["boundary_fused", "moe_combine_boundary", "moe_route", "qk_norm", "sync_status",
+__all__ = ["boundary_fused", "moe_combine_boundary", "boundary_fused_nvfp4",
+           "moe_combine_boundary_nvfp4", "moe_route", "qk_norm", "sync_status",
            "exact_sum_count",
            "version", "BeamError", "LaunchOpts", "library"]
 
@@ -125,6 +126,68 @@ def moe_combine_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: floa
     if st != 0:
         raise BeamError(st, "beam_moe_combine_boundary")
     return y
+
+
+def _nvfp4_out(h, q, sf):
+    import torch
+    T, D = h.shape
+    if D % 16:
+        raise ValueError("NVFP4 output needs D to be a multiple of 16")
+    if q is None:
+        q = torch.empty((T, D // 2), dtype=torch.uint8, device=h.device)
+    if sf is None:
+        sf = torch.empty((T, D // 16), dtype=torch.uint8, device=h.device)
+    _check(q, "y_fp4", torch.uint8, 2)
+    _check(sf, "y_scale", torch.uint8, 2)
+    if tuple(q.shape) != (T, D // 2) or tuple(sf.shape) != (T, D // 16):
+        raise ValueError("shape mismatch: y_fp4 [T, D/2]; y_scale [T, D/16]")
+    return q, sf
+
+
+def boundary_fused_nvfp4(h, x, post_w, pre_w, n: int, eps: float, y_global_scale: float,
+                         y_fp4=None, y_scale=None, stream=None, opts=None):
+    """Dense boundary with y as NVFP4; updates h in place, returns (y_fp4 [T, D/2] uint8,
+    y_scale [T, D/16] uint8)."""
+    import torch
+    for t, name in ((h, "h"), (x, "x")):
+        _check(t, name, torch.bfloat16, 2)
+    _check(post_w, "post_w", torch.bfloat16, 1)
+    _check(pre_w, "pre_w", torch.bfloat16, 1)
+    T, D = h.shape
+    if x.shape != h.shape or post_w.shape[0] != D or pre_w.shape[0] != D:
+        raise ValueError("shape mismatch: h, x [T, D]; post_w, pre_w [D]")
+    q, sf = _nvfp4_out(h, y_fp4, y_scale)
+    st = _lib.load().beam_boundary_fused_nvfp4(_stream_ptr(stream), h.data_ptr(), x.data_ptr(),
+                                               post_w.data_ptr(), pre_w.data_ptr(), int(n),
+                                               float(eps), T, D, float(y_global_scale),
+                                               q.data_ptr(), sf.data_ptr(), _opts(opts))
+    if st != 0:
+        raise BeamError(st, "beam_boundary_fused_nvfp4")
+    return q, sf
+
+
+def moe_combine_boundary_nvfp4(h, expert_out, topk_w, post_w, pre_w, n: int, eps: float,
+                               y_global_scale: float, y_fp4=None, y_scale=None, stream=None,
+                               opts=None):
+    """MoE boundary with y as NVFP4; updates h in place, returns (y_fp4, y_scale)."""
+    import torch
+    _check(h, "h", torch.bfloat16, 2)
+    _check(expert_out, "expert_out", torch.bfloat16, 3)
+    _check(topk_w, "topk_w", torch.float32, 2)
+    _check(post_w, "post_w", torch.bfloat16, 1)
+    _check(pre_w, "pre_w", torch.bfloat16, 1)
+    T, D = h.shape
+    if (expert_out.shape != (T, _lib.BEAM_MOE_TOPK, D) or topk_w.shape != (T, _lib.BEAM_MOE_TOPK)
+            or post_w.shape[0] != D or pre_w.shape[0] != D):
+        raise ValueError("shape mismatch: h [T, D]; expert_out [T, 8, D]; topk_w [T, 8]")
+    q, sf = _nvfp4_out(h, y_fp4, y_scale)
+    st = _lib.load().beam_moe_combine_boundary_nvfp4(
+        _stream_ptr(stream), h.data_ptr(), expert_out.data_ptr(), topk_w.data_ptr(),
+        post_w.data_ptr(), pre_w.data_ptr(), int(n), float(eps), T, D, float(y_global_scale),
+        q.data_ptr(), sf.data_ptr(), _opts(opts))
+    if st != 0:
+        raise BeamError(st, "beam_moe_combine_boundary_nvfp4")
+    return q, sf
 
 
 def moe_route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8,

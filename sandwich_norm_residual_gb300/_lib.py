@@ -48,6 +48,10 @@ SIGNATURES = {
                                             _OPTS]),
     "beam_moe_combine_boundary_scaled": (_i32, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _i32, _f32, _i64,
                                                  _i32, _vp]),
+    "beam_boundary_fused_nvfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _f32, _i64, _i32, _f32, _vp,
+                                          _vp, _vp]),
+    "beam_moe_combine_boundary_nvfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _i64, _i32,
+                                                _f32, _vp, _vp, _vp]),
     "beam_moe_route": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "beam_qk_norm": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _f32,
                              _i32]),

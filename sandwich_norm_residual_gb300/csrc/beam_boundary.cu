@@ -10,7 +10,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
+#include <utility>
 
 #include "boundary_kernels.cuh"
 #include "route.cuh"
@@ -57,41 +59,49 @@ DeviceInfo g_dev[kMaxDevices];
 // memory) exist for these vectors-per-thread values
 bool has_full(int vpt) { return vpt >= 2 && vpt <= 5; }
 
-template <int V, int KIND, bool FULL>
+template <int V, int KIND, bool FULL, bool QUANT>
 KernelFn pick() {
-    if (KIND == kDenseRing) return beam::boundary_ring_kernel<V, FULL>;
-    return beam::boundary_kernel<V, KIND == kMoeRegs, FULL>;
+    if constexpr (KIND == kDenseRing) return beam::boundary_ring_kernel<V, FULL>;
+    else return beam::boundary_kernel<V, KIND == kMoeRegs, FULL, QUANT>;
 }
 
-template <int KIND>
+template <int KIND, bool QUANT>
 KernelFn kernel_for(int vpt, bool full) {
     if (full) {
         switch (vpt) {
-        case 2: return pick<2, KIND, true>();
-        case 3: return pick<3, KIND, true>();
-        case 4: return pick<4, KIND, true>();
-        case 5: return pick<5, KIND, true>();
+        case 2: return pick<2, KIND, true, QUANT>();
+        case 3: return pick<3, KIND, true, QUANT>();
+        case 4: return pick<4, KIND, true, QUANT>();
+        case 5: return pick<5, KIND, true, QUANT>();
         default: return nullptr;
         }
     }
     switch (vpt) {
-    case 1: return pick<1, KIND, false>();
-    case 2: return pick<2, KIND, false>();
-    case 3: return pick<3, KIND, false>();
-    case 4: return pick<4, KIND, false>();
-    case 5: return pick<5, KIND, false>();
-    case 6: return pick<6, KIND, false>();
-    case 7: return pick<7, KIND, false>();
-    case 8: return pick<8, KIND, false>();
+    case 1: return pick<1, KIND, false, QUANT>();
+    case 2: return pick<2, KIND, false, QUANT>();
+    case 3: return pick<3, KIND, false, QUANT>();
+    case 4: return pick<4, KIND, false, QUANT>();
+    case 5: return pick<5, KIND, false, QUANT>();
+    case 6: return pick<6, KIND, false, QUANT>();
+    case 7: return pick<7, KIND, false, QUANT>();
+    case 8: return pick<8, KIND, false, QUANT>();
     default: return nullptr;
     }
 }
 
-KernelFn kernel_for_kind(int kind, int vpt, bool full) {
-    return kind == kDenseRing ? kernel_for<kDenseRing>(vpt, full)
-           : kind == kMoeRegs ? kernel_for<kMoeRegs>(vpt, full)
-                              : kernel_for<kDenseRegs>(vpt, full);
+KernelFn kernel_for_kind(int kind, int vpt, bool full, bool quant = false) {
+    if (quant) return kind == kMoeRegs ? kernel_for<kMoeRegs, true>(vpt, full) : kernel_for<kDenseRegs, true>(vpt, full);
+    return kind == kDenseRing ? kernel_for<kDenseRing, false>(vpt, full)
+           : kind == kMoeRegs ? kernel_for<kMoeRegs, false>(vpt, full)
+                              : kernel_for<kDenseRegs, false>(vpt, full);
 }
+
+// NVFP4 destination of y (NULL: y is written as BF16)
+struct QuantOut {
+    uint8_t* q;
+    uint8_t* sf;
+    float gs;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -241,7 +251,8 @@ beam_status check_common(int n, float eps, int64_t T, int D, const beam_launch_o
 
 beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* x, const uint16_t* e,
                    const float* w, const uint16_t* post_w, const uint16_t* pre_w, int n, float eps,
-                   int64_t T, int D, uint16_t* y, const beam_launch_opts* opts, float route_scale = 1.0f) {
+                   int64_t T, int D, uint16_t* y, const beam_launch_opts* opts, float route_scale = 1.0f,
+                   const QuantOut* quant = nullptr) {
     DeviceInfo* info = nullptr;
     beam_status st = current_device(&info);
     if (st != BEAM_OK) return st;
@@ -263,6 +274,7 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
     if (!moe) {
         // dense rows go through the shared-memory ring when at least two slots fit
         int want = (opts && opts->stages) ? opts->stages : kAutoStages;
+        if (quant) want = -1;  // the NVFP4 output exists only in the register kernels
         if (want == -1 && opts && !opts->stages && (opts->flags & BEAM_OPT_TEST_WAIT_TIMEOUT)) want = kTestStages;
         if (want == -1) {
             kind = kDenseRegs;
@@ -285,12 +297,12 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
         }
     }
     if (kind != kDenseRing) {
-        fn = kernel_for_kind(kind, vpt, full);
+        fn = kernel_for_kind(kind, vpt, full, quant != nullptr);
         if (!fn) return BEAM_ERR_SHAPE;
         st = smem_limit(info, fn, &limit);
         if (st != BEAM_OK) return st;
         if (wbytes > limit) {  // weights do not fit: the generic kernel reads them from global memory
-            fn = kernel_for_kind(kind, vpt, false);
+            fn = kernel_for_kind(kind, vpt, false, quant != nullptr);
             if (!fn) return BEAM_ERR_SHAPE;
         }
     }
@@ -328,6 +340,9 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
     p.wait_ns = kWaitNs;
     p.test_wait_ns = kTestWaitNs;
     p.route_scale = route_scale;
+    p.yq = quant ? quant->q : nullptr;
+    p.ysf = quant ? quant->sf : nullptr;
+    p.y_gs = quant ? quant->gs : 0.0f;
 
     void* args[] = {&p};
     cudaError_t err;
@@ -375,6 +390,68 @@ beam_status beam_boundary_fused_ex(beam_stream_t stream, uint16_t* h, const uint
     if ((const void*)x != (const void*)h && overlaps(h, rows, x, rows)) return BEAM_ERR_ALIAS;
     if (overlaps(h, rows, post_w, vec) || overlaps(h, rows, pre_w, vec)) return BEAM_ERR_ALIAS;
     return launch(false, stream, h, x, nullptr, nullptr, post_w, pre_w, n, eps, T, D, y_out, opts);
+}
+
+static beam_status check_nvfp4(int64_t T, int D, float gs, const uint8_t* q, const uint8_t* sf,
+                               const beam_launch_opts* opts) {
+    if (D % 16) return BEAM_ERR_SHAPE;
+    // the register kernels alone write NVFP4: no ring options
+    if (opts && (opts->stages > 0 || (opts->flags & BEAM_OPT_TEST_WAIT_TIMEOUT))) return BEAM_ERR_ARG;
+    if (!(gs > 0.0f) || !std::isfinite(gs)) return BEAM_ERR_ARG;
+    if (T > 0 && (!q || !sf)) return BEAM_ERR_NULL;
+    if (T > 0 && !aligned16(q)) return BEAM_ERR_ALIGN;
+    if (overlaps(q, (size_t)T * D / 2, sf, (size_t)T * D / 16)) return BEAM_ERR_ALIAS;
+    return BEAM_OK;
+}
+
+// y's NVFP4 buffers against every other operand
+static bool nvfp4_overlaps(const uint8_t* q, const uint8_t* sf, int64_t T, int D,
+                           std::initializer_list<std::pair<const void*, size_t>> others) {
+    for (const auto& o : others)
+        if (overlaps(q, (size_t)T * D / 2, o.first, o.second) || overlaps(sf, (size_t)T * D / 16, o.first, o.second))
+            return true;
+    return false;
+}
+
+beam_status beam_boundary_fused_nvfp4(beam_stream_t stream, uint16_t* h, const uint16_t* x, const uint16_t* post_w,
+                                      const uint16_t* pre_w, int n, float eps, int64_t T, int D,
+                                      float y_global_scale, uint8_t* y_fp4, uint8_t* y_scale,
+                                      const beam_launch_opts* opts) {
+    beam_status st = check_common(n, eps, T, D, opts);
+    if (st == BEAM_OK) st = check_nvfp4(T, D, y_global_scale, y_fp4, y_scale, opts);
+    if (st != BEAM_OK || T == 0) return st;
+    if (!h || !x || !post_w || !pre_w) return BEAM_ERR_NULL;
+    if (!aligned16(h) || !aligned16(x) || !aligned16(post_w) || !aligned16(pre_w)) return BEAM_ERR_ALIGN;
+    const size_t rows = (size_t)T * (size_t)D * 2u, vec = (size_t)D * 2u;
+    if (nvfp4_overlaps(y_fp4, y_scale, T, D, {{h, rows}, {x, rows}, {post_w, vec}, {pre_w, vec}}))
+        return BEAM_ERR_ALIAS;
+    if ((const void*)x != (const void*)h && overlaps(h, rows, x, rows)) return BEAM_ERR_ALIAS;
+    if (overlaps(h, rows, post_w, vec) || overlaps(h, rows, pre_w, vec)) return BEAM_ERR_ALIAS;
+    const QuantOut qo{y_fp4, y_scale, y_global_scale};
+    return launch(false, stream, h, x, nullptr, nullptr, post_w, pre_w, n, eps, T, D, nullptr, opts, 1.0f, &qo);
+}
+
+beam_status beam_moe_combine_boundary_nvfp4(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,
+                                            const float* topk_w, const uint16_t* post_w, const uint16_t* pre_w,
+                                            int n, float eps, int64_t T, int D, float y_global_scale,
+                                            uint8_t* y_fp4, uint8_t* y_scale, const beam_launch_opts* opts) {
+    beam_status st = check_common(n, eps, T, D, opts);
+    if (st == BEAM_OK) st = check_nvfp4(T, D, y_global_scale, y_fp4, y_scale, opts);
+    if (st != BEAM_OK || T == 0) return st;
+    if (!h || !expert_out || !topk_w || !post_w || !pre_w) return BEAM_ERR_NULL;
+    if (!aligned16(h) || !aligned16(expert_out) || !aligned16(topk_w) || !aligned16(post_w) || !aligned16(pre_w))
+        return BEAM_ERR_ALIGN;
+    const size_t rows = (size_t)T * (size_t)D * 2u, vec = (size_t)D * 2u;
+    const size_t erows = rows * BEAM_MOE_TOPK, wbytes = (size_t)T * BEAM_MOE_TOPK * 4u;
+    if (nvfp4_overlaps(y_fp4, y_scale, T, D,
+                       {{h, rows}, {expert_out, erows}, {topk_w, wbytes}, {post_w, vec}, {pre_w, vec}}))
+        return BEAM_ERR_ALIAS;
+    if (overlaps(h, rows, expert_out, erows) || overlaps(h, rows, topk_w, wbytes) || overlaps(h, rows, post_w, vec) ||
+        overlaps(h, rows, pre_w, vec))
+        return BEAM_ERR_ALIAS;
+    const QuantOut qo{y_fp4, y_scale, y_global_scale};
+    return launch(true, stream, h, nullptr, expert_out, topk_w, post_w, pre_w, n, eps, T, D, nullptr, opts, 1.0f,
+                  &qo);
 }
 
 beam_status beam_boundary_fused(beam_stream_t stream, uint16_t* h, const uint16_t* x, const uint16_t* post_w,

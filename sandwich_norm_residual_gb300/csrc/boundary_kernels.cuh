@@ -42,6 +42,9 @@ struct BoundaryParams {
     unsigned long long wait_ns;       // bound of every mbarrier wait
     unsigned long long test_wait_ns;  // bound of the test hook's wait
     float route_scale;      // MoE: x = bf16(route_scale * acc); 1 when the weights carry it
+    uint8_t* yq;            // NVFP4 y: [T, D/2] E2M1 codes, element 2i in the low nibble
+    uint8_t* ysf;           // NVFP4 y: [T, D/16] E4M3 block scales
+    float y_gs;             // NVFP4 y: global scale
 };
 
 constexpr unsigned kFlagForceExact = 1u;
@@ -175,6 +178,37 @@ __device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
     return d;
 }
 
+// FP32 -> E4M3 (OCP E4M3FN), nearest even, saturating; the code in the low byte
+__device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
+    uint32_t r;
+    asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; cvt.u32.u16 %0, t; }" : "=r"(r) : "f"(0.0f), "f"(v));
+    return r & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+    float f;
+    const unsigned short b = (unsigned short)code;
+    asm("{ .reg .b32 t; .reg .b16 lo, hi; cvt.rn.f16x2.e4m3x2 t, %1; mov.b32 {lo, hi}, t; cvt.f32.f16 %0, lo; }"
+        : "=f"(f) : "h"(b));
+    return f;
+}
+
+// two FP32 -> two E2M1 codes, nearest even, saturating: lo in bits 0-3, hi in 4-7
+__device__ __forceinline__ uint32_t f2_to_e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// h is read and later overwritten by the same thread; this form also keeps
+// the read ahead of any later store (the NVFP4 MoE path parks x in the h row)
+__device__ __forceinline__ uint4 ld_stream_rw_ordered(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
+    return r;
+}
+
 __device__ __forceinline__ float rms_factor(float S, int D, float eps) {
     float ms = __fdiv_rn(S, (float)D);
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
@@ -221,7 +255,7 @@ __device__ __forceinline__ void load_weights(const uint16_t* g, const float* ws,
 // `after_s1` runs on every thread right after the post-norm reduction's
 // barrier, when every thread has consumed its inputs of this row. FULL: the
 // row is exactly NT * VPT vectors (no bounds checks) and ws holds the weights.
-template <int VPT, bool MOE, bool FULL, class AfterS1>
+template <int VPT, bool MOE, bool FULL, bool QUANT, class AfterS1>
 __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long row, uint4 (&xv)[VPT],
                                            uint4 (&hv)[VPT], RedScratch* rs, ExactScratch* sc,
                                            const float* ws, AfterS1 after_s1) {
@@ -247,13 +281,16 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
         // or, for MoE, the combined x parked in this y row
         const uint16_t* srow = p.x + base;
         if (MOE) {
+            // park x in this row of y, or, when y leaves as NVFP4, in the row of
+            // h (already in registers; h' overwrites it later)
+            uint16_t* park = QUANT ? p.h + base : p.y + base;
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int vi = tid + i * nt;
-                if (FULL || vi < p.nvec) st_stream(p.y + base + (size_t)vi * 8, xv[i]);
+                if (FULL || vi < p.nvec) st_stream(park + (size_t)vi * 8, xv[i]);
             }
             __syncthreads();
-            srow = p.y + base;
+            srow = park;
         }
         S1 = exact_row_sum_squares(srow, p.D, sc);
     }
@@ -295,18 +332,44 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
     const float r2 = rms_factor(S2, p.D, p.eps);
     const float2 r2v = make_float2(r2, r2);
 
-    // ---- y = bf16((h' r2) pre_w)
+    // ---- y = bf16((h' r2) pre_w), stored as BF16 or quantised to NVFP4
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int vi = tid + i * nt;
-        if (FULL || vi < p.nvec) {
+        const bool valid = FULL || vi < p.nvec;
+        uint4 yv = make_uint4(0, 0, 0, 0);
+        if (valid) {
             float2 qw[4];
             load_weights<FULL>(p.pre_w, ws ? ws + p.D : nullptr, vi, qw);
-            uint4 yv;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 set_word(yv, q, f2_to_bf2(mul2_rn(mul2_rn(bf2_to_f2(word(hv[i], q)), r2v), qw[q])));
-            st_stream(p.y + base + (size_t)vi * 8, yv);
+            if (!QUANT) st_stream(p.y + base + (size_t)vi * 8, yv);
+        }
+        if (QUANT) {
+            // a block of 16 is this vector and its neighbour, held by lane ^ 1
+            float am = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = bf2_to_f2(word(yv, q));
+                am = fmaxf(am, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+            const uint32_t sfb = f32_to_e4m3(__fmul_rn(__fdiv_rn(am, 6.0f), p.y_gs));
+            const float sfv = e4m3_to_f32(sfb);
+            uint32_t codes = 0u;
+            if (sfv != 0.0f) {
+                const float inv = __fdiv_rn(p.y_gs, sfv);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = bf2_to_f2(word(yv, q));
+                    codes |= f2_to_e2m1x2(__fmul_rn(f.x, inv), __fmul_rn(f.y, inv)) << (8 * q);
+                }
+            }
+            if (valid) {
+                *reinterpret_cast<uint32_t*>(p.yq + (base + (size_t)vi * 8) / 2) = codes;
+                if (!(vi & 1)) p.ysf[(base + (size_t)vi * 8) / 16] = (uint8_t)sfb;
+            }
         }
     }
 }
@@ -317,7 +380,7 @@ struct NoOp {
 
 // Loads straight to registers (dense x or the MoE combine), optionally asking
 // L2 for the inputs of this CTA's row `prefetch_rows` ahead.
-template <int VPT, bool MOE, bool FULL>
+template <int VPT, bool MOE, bool FULL, bool QUANT>
 __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryParams p) {
     extern __shared__ __align__(16) float ws_dyn[];
     __shared__ RedScratch rs;
@@ -380,9 +443,11 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int vi = tid + i * nt;
-            hv[i] = (FULL || vi < p.nvec) ? ld_stream_rw(p.h + base + (size_t)vi * 8) : make_uint4(0, 0, 0, 0);
+            const uint16_t* hp = p.h + base + (size_t)vi * 8;
+            hv[i] = (FULL || vi < p.nvec) ? ((MOE && QUANT) ? ld_stream_rw_ordered(hp) : ld_stream_rw(hp))
+                                         : make_uint4(0, 0, 0, 0);
         }
-        finish_row<VPT, MOE, FULL>(p, row, xv, hv, &rs, &sc, ws, NoOp{});
+        finish_row<VPT, MOE, FULL, QUANT>(p, row, xv, hv, &rs, &sc, ws, NoOp{});
     }
 }
 
@@ -451,7 +516,7 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const Bounda
             xv[j] = (FULL || vi < p.nvec) ? xs[vi] : make_uint4(0, 0, 0, 0);
             hv[j] = (FULL || vi < p.nvec) ? hs[vi] : make_uint4(0, 0, 0, 0);
         }
-        finish_row<VPT, false, FULL>(p, blockIdx.x + i * G, xv, hv, &rs, &sc, ws, [&]() {
+        finish_row<VPT, false, FULL, false>(p, blockIdx.x + i * G, xv, hv, &rs, &sc, ws, [&]() {
             if (tid == 0 && !dead && i + S < n_iter) issue(i + S);
         });
     }

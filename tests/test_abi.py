@@ -215,3 +215,35 @@ def test_qk_norm_argument_errors(lib):
     assert qk(k=Q + 4 * 48 * 128 * 2 - 256) == _lib.BEAM_ERR_ALIAS
     # SSMax needs no table
     assert qk(mode=1, tb=None, max_pos=0) != _lib.BEAM_ERR_NULL
+
+
+def test_nvfp4_argument_errors(lib):
+    H, X, PW, QW, Q, SF = (A + (i << 32) for i in range(6))
+    E, W = A + (6 << 32), A + (7 << 32)
+
+    def dense(T=4, d=D, gs=100.0, h=H, x=X, q=Q, sf=SF, opts=None):
+        return lib.beam_boundary_fused_nvfp4(None, h, x, PW, QW, 2, 1e-6, T, d, gs, q, sf, opts)
+
+    def moe(T=4, d=D, gs=100.0, h=H, q=Q, sf=SF, w=W, opts=None):
+        return lib.beam_moe_combine_boundary_nvfp4(None, h, E, w, PW, QW, 2, 1e-6, T, d, gs, q, sf, opts)
+
+    assert dense(d=520) == _lib.BEAM_ERR_SHAPE       # a multiple of 8, not of 16
+    assert moe(d=520) == _lib.BEAM_ERR_SHAPE
+    for gs in (0.0, -1.0, float("inf"), float("nan")):
+        assert dense(gs=gs) == _lib.BEAM_ERR_ARG
+        assert moe(gs=gs) == _lib.BEAM_ERR_ARG
+    assert dense(T=0, h=None, q=None, sf=None) == _lib.BEAM_OK
+    assert dense(q=None) == _lib.BEAM_ERR_NULL
+    assert moe(sf=None) == _lib.BEAM_ERR_NULL
+    assert dense(q=Q + 8) == _lib.BEAM_ERR_ALIGN
+    assert dense(sf=Q + 4 * D // 2 - 1) == _lib.BEAM_ERR_ALIAS   # scales over the codes
+    assert dense(q=X + 64) == _lib.BEAM_ERR_ALIAS                # codes inside x
+    assert dense(sf=H + 2) == _lib.BEAM_ERR_ALIAS                # scales inside h
+    assert moe(q=E + 4096) == _lib.BEAM_ERR_ALIAS                # codes inside the experts
+    assert moe(sf=W + 8) == _lib.BEAM_ERR_ALIAS                  # scales inside the weights
+    assert dense(x=H) != _lib.BEAM_ERR_ALIAS                     # x may be h itself
+    ring = _lib.LaunchOpts(stages=2)
+    hook = _lib.LaunchOpts(flags=_lib.BEAM_OPT_TEST_WAIT_TIMEOUT)
+    assert dense(opts=ctypes.byref(ring)) == _lib.BEAM_ERR_ARG     # the ring writes no NVFP4
+    assert dense(opts=ctypes.byref(hook)) == _lib.BEAM_ERR_ARG
+    assert moe(opts=ctypes.byref(_lib.LaunchOpts(reserved=(0, 1, 0)))) == _lib.BEAM_ERR_ARG

@@ -87,8 +87,8 @@ MUTANTS = [
      "q[(blk * 16 + j) / 2] = (uint8_t)(hi | (lo << 4));"),
     ("FP8/FP4 ties away from zero", "if (d < bd || (d == bd && (c & 1u) == 0 && (best & 1u))) { best = c; bd = d; }",
      "if (d < bd || (d == bd && c > best)) { best = c; bd = d; }"),
-    ("NVFP4 quantises with the global scale inverted", "float a = (oracle_bf16_to_f32(y[blk * 16 + j]) * gs) / sv;",
-     "float a = (oracle_bf16_to_f32(y[blk * 16 + j]) / gs) / sv;"),
+    ("NVFP4 quantises with the global scale inverted", "const float inv = sv != 0.0f ? gs / sv : 0.0f;",
+     "const float inv = sv != 0.0f ? 1.0f / (gs * sv) : 0.0f;"),
     ("long-double residual coefficient squared",
      "long double c1 = sqrtl((long double)(n - 1) / (long double)n);\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i",
      "long double c1 = (long double)(n - 1) / (long double)n;\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i"),

@@ -755,3 +755,25 @@ def test_nvfp4_dequantises_within_half_a_step():
         # scale rounding (E4M3, 4 significant bits) may clip the top value a little; the
         # grid step near amax is 2 (in scaled units) -> half a step is amax/6, plus clipping
         assert np.all(np.abs(deq - seg) <= amax / 6 + 2 ** -4 * amax + 1e-12)
+
+
+def test_nvfp4_boundaries_are_the_bf16_boundaries_then_the_row_quantiser():
+    rng = np.random.default_rng(92)
+    T, D, n, eps, gs = 6, 512, 5, 1e-6, 336.0
+    h = bf16_bits(rng.standard_normal((T, D)))
+    x = bf16_bits(rng.standard_normal((T, D)))
+    pw, qw = bf16_bits(1 + 0.1 * rng.standard_normal(D)), bf16_bits(1 + 0.1 * rng.standard_normal(D))
+    h1, y = oracle.boundary(h, x, pw, qw, n, eps)
+    h2, q, sf = oracle.boundary_nvfp4(h, x, pw, qw, n, eps, gs)
+    assert np.array_equal(h1, h2)
+    for t in range(T):
+        qr, sr = oracle.nvfp4_row(y[t], gs)
+        assert np.array_equal(q[t], qr) and np.array_equal(sf[t], sr)
+    e = bf16_bits(rng.standard_normal((T, 8, D)))
+    w = rng.uniform(0, 0.4, (T, 8)).astype(np.float32)
+    h1, y = oracle.moe_boundary(h, e, w, pw, qw, n, eps)
+    h2, q, sf = oracle.moe_boundary_nvfp4(h, e, w, pw, qw, n, eps, gs)
+    assert np.array_equal(h1, h2)
+    for t in range(T):
+        qr, sr = oracle.nvfp4_row(y[t], gs)
+        assert np.array_equal(q[t], qr) and np.array_equal(sf[t], sr)

@@ -560,3 +560,142 @@ def test_qk_norm_forced_exact_path_and_bad_positions():
     keep = torch.arange(64) != 3
     assert torch.equal(c[0][keep], a[0][keep])
     snr.sync_status()  # cleared
+
+
+# --------------------------------------------------------------- y as NVFP4
+
+def gpu_dense_nvfp4(inp, n, eps, gs, opts=None, stream=None):
+    d = to_dev(inp)
+    q, sf = snr.boundary_fused_nvfp4(d["h"], d["x"], d["post_w"], d["pre_w"], n, eps, gs,
+                                     opts=opts, stream=stream)
+    snr.sync_status(stream)
+    return bits(d["h"]), q.cpu().numpy(), sf.cpu().numpy()
+
+
+def gpu_moe_nvfp4(inp, n, eps, gs, opts=None):
+    d = to_dev(inp)
+    q, sf = snr.moe_combine_boundary_nvfp4(d["h"], d["expert_out"], d["topk_w"], d["post_w"],
+                                           d["pre_w"], n, eps, gs, opts=opts)
+    snr.sync_status()
+    return bits(d["h"]), q.cpu().numpy(), sf.cpu().numpy()
+
+
+def check_nvfp4(got, want, label):
+    """h' bit for bit; every E2M1 code byte and E4M3 scale byte identical."""
+    assert_parity(got[0], want[0], f"{label} h'")
+    for g, w, name in ((got[1], want[1], "codes"), (got[2], want[2], "scales")):
+        assert g.shape == w.shape, (label, name, g.shape, w.shape)
+        bad = np.argwhere(g != w)
+        assert bad.size == 0, (f"{label} {name}: {len(bad)} of {g.size} bytes differ, first at "
+                               f"{bad[:4].tolist()}: got {g[tuple(bad[0])]:#04x} "
+                               f"want {w[tuple(bad[0])]:#04x}")
+    print(f"{label}: h' identical, {got[1].size} code bytes and {got[2].size} scales identical")
+
+
+# 448 * 6 / amax(y) with amax(y) near 8 is the usual per-tensor scale; the
+# others drive the E4M3 scales subnormal, to zero, and into saturation
+GLOBAL_SCALES = (336.0, 1.0, 1e-3, 1e5)
+
+
+def test_nvfp4_dense_prefill_full():
+    cfg = CONFIGS[2]
+    inp = synth.dense_inputs(cfg)
+    want = oracle.boundary_nvfp4(inp["h"], inp["x"], inp["post_w"], inp["pre_w"], cfg.n, cfg.eps,
+                                 336.0, threads=THREADS)
+    check_nvfp4(gpu_dense_nvfp4(inp, cfg.n, cfg.eps, 336.0), want, f"{cfg.name} nvfp4")
+
+
+def test_nvfp4_moe_full():
+    cfg = CONFIGS[3]
+    inp = synth.moe_inputs(cfg)
+    want = oracle.moe_boundary_nvfp4(inp["h"], inp["expert_out"], inp["topk_w"], inp["post_w"],
+                                     inp["pre_w"], cfg.n, cfg.eps, 336.0, threads=THREADS)
+    check_nvfp4(gpu_moe_nvfp4(inp, cfg.n, cfg.eps, 336.0), want, f"{cfg.name} nvfp4")
+
+
+@pytest.mark.parametrize("gs", GLOBAL_SCALES)
+def test_nvfp4_global_scales_and_zero_and_outlier_rows(gs):
+    T, D = 40, 5120
+    inp = random_dense(T, D, seed=21)
+    x = inp["x"].float()
+    x[0] = 0.0          # y is pre_w-scaled h' alone
+    x[1] *= 100.0       # outlier branch
+    x[2, ::16] *= 3e4   # one huge element in every block
+    inp["x"] = x.to(torch.bfloat16)
+    h = inp["h"].float()
+    h[3] = 0.0
+    h[3, 17] = 1.0      # one non-zero block in a row
+    h[4, :32] = 0.0     # whole blocks of zeros: sf = 0
+    inp["h"] = h.to(torch.bfloat16)
+    want = oracle.boundary_nvfp4(inp["h"], inp["x"], inp["post_w"], inp["pre_w"], 3, 1e-6, gs)
+    check_nvfp4(gpu_dense_nvfp4(inp, 3, 1e-6, gs), want, f"nvfp4 gs={gs}")
+
+
+@pytest.mark.parametrize("T,D,n", [(1, 16, 2), (5, 48, 3), (257, 528, 7), (3, 5136, 104),
+                                   (17, 16384, 11), (2, 32768, 5)])
+def test_nvfp4_shapes(T, D, n):
+    inp = random_dense(T, D, seed=T * 31 + D)
+    want = oracle.boundary_nvfp4(inp["h"], inp["x"], inp["post_w"], inp["pre_w"], n, 1e-6, 336.0)
+    check_nvfp4(gpu_dense_nvfp4(inp, n, 1e-6, 336.0), want, f"nvfp4 T={T} D={D}")
+    rng = np.random.default_rng(D)
+    m = dict(h=inp["h"], expert_out=bf16(rng.standard_normal((T, 8, D))),
+             topk_w=torch.from_numpy(rng.uniform(0, 0.4, (T, 8)).astype(np.float32)),
+             post_w=inp["post_w"], pre_w=inp["pre_w"])
+    want = oracle.moe_boundary_nvfp4(m["h"], m["expert_out"], m["topk_w"], m["post_w"], m["pre_w"],
+                                     n, 1e-6, 336.0)
+    check_nvfp4(gpu_moe_nvfp4(m, n, 1e-6, 336.0), want, f"moe nvfp4 T={T} D={D}")
+
+
+def test_nvfp4_launch_shapes_forced_exact_and_pdl():
+    """Every vectors-per-thread choice, the exact row-sum path (for MoE it parks
+    the combined x in the h row), and PDL give the same bytes."""
+    T, D = 96, 5120
+    inp = random_dense(T, D, seed=22)
+    want = oracle.boundary_nvfp4(inp["h"], inp["x"], inp["post_w"], inp["pre_w"], 9, 1e-6, 336.0)
+    force, pdl = snr._lib.BEAM_OPT_FORCE_EXACT_SUM, snr._lib.BEAM_OPT_PDL
+    for v in (2, 3, 4, 5, 6, 7, 8):
+        for flags in (0, force, pdl):
+            got = gpu_dense_nvfp4(inp, 9, 1e-6, 336.0, opts=dict(vec_per_thread=v, flags=flags))
+            check_nvfp4(got, want, f"dense nvfp4 vpt={v} flags={flags}")
+    cfg = CONFIGS[3]
+    m = synth.moe_inputs(cfg, rows=64)
+    want = oracle.moe_boundary_nvfp4(m["h"], m["expert_out"], m["topk_w"], m["post_w"],
+                                     m["pre_w"], cfg.n, cfg.eps, 336.0)
+    for v in (2, 3, 4, 5, 8):
+        for flags in (0, force, pdl):
+            snr.exact_sum_count(reset=True)
+            got = gpu_moe_nvfp4(m, cfg.n, cfg.eps, 336.0, opts=dict(vec_per_thread=v, flags=flags))
+            if flags == force:
+                assert snr.exact_sum_count() == 2 * 64
+            check_nvfp4(got, want, f"moe nvfp4 vpt={v} flags={flags}")
+
+
+def test_nvfp4_agrees_with_quantising_the_bf16_output():
+    """The quantised call equals the BF16 call followed by the oracle's NVFP4
+    quantiser on its y, row by row."""
+    cfg = CONFIGS[3]
+    m = synth.moe_inputs(cfg, rows=128)
+    h_bf, y_bf = gpu_moe(m, cfg.n, cfg.eps)
+    h_q, q, sf = gpu_moe_nvfp4(m, cfg.n, cfg.eps, 336.0)
+    assert np.array_equal(h_bf, h_q)
+    for t in range(y_bf.shape[0]):
+        qr, sr = oracle.nvfp4_row(y_bf[t], 336.0)
+        assert np.array_equal(q[t], qr) and np.array_equal(sf[t], sr), t
+
+
+def test_nvfp4_branch_is_the_stream_guard_bands_and_zero_tokens():
+    T, D = 21, 5120
+    inp = random_dense(T, D, seed=23)
+    d = to_dev(inp)
+    qbuf = torch.full((T + 2, D // 2), 0xA5, dtype=torch.uint8, device=DEV)
+    sbuf = torch.full((T + 2, D // 16), 0xA5, dtype=torch.uint8, device=DEV)
+    q, sf = snr.boundary_fused_nvfp4(d["h"], d["h"], d["post_w"], d["pre_w"], 6, 1e-6, 336.0,
+                                     y_fp4=qbuf[1:T + 1], y_scale=sbuf[1:T + 1])
+    snr.sync_status()
+    for b in (qbuf, sbuf):
+        assert (b[0] == 0xA5).all() and (b[-1] == 0xA5).all()
+    want = oracle.boundary_nvfp4(inp["h"], inp["h"], inp["post_w"], inp["pre_w"], 6, 1e-6, 336.0)
+    check_nvfp4((bits(d["h"]), q.cpu().numpy(), sf.cpu().numpy()), want, "nvfp4 x is h")
+    h0 = torch.zeros((0, D), dtype=torch.bfloat16, device=DEV)
+    q0, s0 = snr.boundary_fused_nvfp4(h0, h0, d["post_w"], d["pre_w"], 2, 1e-6, 336.0)
+    assert q0.shape == (0, D // 2) and s0.shape == (0, D // 16)
