@@ -251,28 +251,101 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
     return {k: round(v, 2) for k, v in out.items()}
 
 
-def route_latency(snr, device, reps: int = 50) -> float:
-    """Group-limited top-8 routing of T = 16384 tokens (256 experts, 8 groups, keep 4),
-    microseconds per launch; reported beside the step, which it is not part of."""
+def nvfp4_bytes(T: int, moe: bool) -> int:
+    # as the BF16 boundaries, with y written as D/2 code bytes + D/16 scale bytes
+    y_bf16, y_fp4 = 2 * D, D // 2 + D // 16
+    return (moe_bytes(T) if moe else dense_bytes(T)) - T * y_bf16 + T * y_fp4
+
+
+QK_HEADS, QK_KV_HEADS, QK_DIM, QK_SEQ = 48, 8, 128, 2048
+
+
+def qk_bytes(T: int, rope: bool) -> int:
+    # q and k read and written in place, one position per token, the two weight
+    # vectors; RoPE also reads the cos|sin table once (2048 positions x 128 FP32)
+    b = T * ((QK_HEADS + QK_KV_HEADS) * QK_DIM * 2 * 2 + 4) + 2 * QK_DIM * 2
+    return b + (QK_SEQ * QK_DIM * 4 if rope else 0)
+
+
+def route_bytes(T: int) -> int:
+    return T * (256 * 4 + 8 * 8) + 256 * 4   # FP32 logits in; ids and weights out; bias
+
+
+def _time_launches(fn, stream, reps: int, warmup: int = 3) -> float:
+    """Mean microseconds per launch, CUDA events on the launching stream."""
     import torch
-    import synth
-    z = (synth.normal(3, 8, T_TOKENS * 256) * 2.0).reshape(T_TOKENS, 256)
-    b = synth.normal(3, 9, 256) * 0.05
-    zt, bt = torch.from_numpy(z).to(device), torch.from_numpy(b).to(device)
-    idx = torch.empty((T_TOKENS, 8), dtype=torch.int32, device=device)
-    w = torch.empty((T_TOKENS, 8), dtype=torch.float32, device=device)
-    stream = torch.cuda.Stream(device)
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            snr.moe_route(zt, bt, idx=idx, w=w, stream=stream)
+        for i in range(warmup):
+            fn(i)
         a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(reps):
-            snr.moe_route(zt, bt, idx=idx, w=w, stream=stream)
+        for i in range(reps):
+            fn(i)
         e.record(stream)
-    torch.cuda.synchronize(device)
+    torch.cuda.synchronize()
+    return a.elapsed_time(e) * 1e3 / reps
+
+
+def next_rows(snr, device, dev, peak: float) -> dict:
+    """The scope table's next rows at T = 16384, each timed on its own and
+    reported beside the step (none is part of it): group-limited top-8 routing,
+    per-head Q/K norm with RoPE or SSMax (8 sequences of 2048 positions), and
+    the two boundaries with y written as NVFP4."""
+    import torch
+    import synth
+    stream = torch.cuda.Stream(device)
+    T = T_TOKENS
+    out = {}
+
+    def entry(us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"us": round(us, 2), "bytes": nbytes, "GBps": round(gbs, 1),
+                "frac_of_measured_hbm": round(gbs / peak, 4)}
+
+    # routing: ten logit buffers in turn, so each launch reads from DRAM (L2 holds one)
+    nbuf = 10
+    z = torch.from_numpy((synth.normal(3, 8, nbuf * T * 256) * 2.0).reshape(nbuf, T, 256)).to(device)
+    b = torch.from_numpy(synth.normal(3, 9, 256) * 0.05).to(device)
+    idx = torch.empty((T, 8), dtype=torch.int32, device=device)
+    w = torch.empty((T, 8), dtype=torch.float32, device=device)
+    us = _time_launches(lambda i: snr.moe_route(z[i % nbuf], b, idx=idx, w=w, stream=stream),
+                        stream, 50)
+    out["route_top8_of_256"] = entry(us, route_bytes(T))
+    del z
+
+    # Q/K norm: q [T, 48, 128] and k [T, 8, 128] (235 MB together, above L2)
+    q = torch.from_numpy((synth.normal(3, 10, T * QK_HEADS * QK_DIM) * 2.0)
+                         .reshape(T, QK_HEADS, QK_DIM)).to(device).to(torch.bfloat16)
+    k = torch.from_numpy((synth.normal(3, 11, T * QK_KV_HEADS * QK_DIM) * 2.0)
+                         .reshape(T, QK_KV_HEADS, QK_DIM)).to(device).to(torch.bfloat16)
+    qw = torch.from_numpy(1 + 0.1 * synth.normal(3, 12, QK_DIM)).to(device).to(torch.bfloat16)
+    kw = torch.from_numpy(1 + 0.1 * synth.normal(3, 13, QK_DIM)).to(device).to(torch.bfloat16)
+    pos = (torch.arange(T, dtype=torch.int32, device=device) % QK_SEQ).contiguous()
+    inv = 10000.0 ** (-torch.arange(0, QK_DIM, 2, dtype=torch.float64) / QK_DIM)
+    ang = torch.arange(QK_SEQ, dtype=torch.float64)[:, None] * inv[None, :]
+    table = torch.cat([ang.cos(), ang.sin()], 1).float().to(device).contiguous()
+    for mode in ("rope", "ssmax"):
+        us = _time_launches(lambda i, mode=mode: snr.qk_norm(
+            q, k, qw, kw, pos, 1e-6, mode=mode, rope_table=table if mode == "rope" else None,
+            stream=stream), stream, 20)
+        out[f"qk_norm_{mode}"] = entry(us, qk_bytes(T, mode == "rope"))
+    del q, k
+
+    # the boundaries with y as NVFP4, on the step's own buffers
+    dn, mo = dev["dense"], dev["moe"]
+    gs = 336.0
+    yq = torch.empty((T, D // 2), dtype=torch.uint8, device=device)
+    ys = torch.empty((T, D // 16), dtype=torch.uint8, device=device)
+    us = _time_launches(lambda i: snr.boundary_fused_nvfp4(
+        dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, gs, y_fp4=yq, y_scale=ys,
+        stream=stream), stream, 20)
+    out["dense_boundary_nvfp4"] = entry(us, nvfp4_bytes(T, False))
+    us = _time_launches(lambda i: snr.moe_combine_boundary_nvfp4(
+        mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"], mo["pre_w"], MOE_N, EPS, gs,
+        y_fp4=yq, y_scale=ys, stream=stream), stream, 20)
+    out["moe_boundary_nvfp4"] = entry(us, nvfp4_bytes(T, True))
     snr.sync_status(stream)
-    return round(a.elapsed_time(e) * 1e3 / reps, 2)
+    return out
 
 
 def bench_ours(args, rank, world, local_rank):
@@ -335,15 +408,42 @@ def bench_ours(args, rank, world, local_rank):
     dense_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     moe_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
 
-    # end to end through the public API: pinned host inputs in, results out, every step
+    # end to end through the public API with the batch in host memory: page-locked
+    # inputs and outputs that the kernels read and write over the CPU-GPU link
+    # (beam_*_host); h' overwrites h in host memory, y lands in host memory
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    out_host = {g: {k: torch.empty_like(host[g]["h"], device="cpu").pin_memory() for k in ("h", "y")}
-                for g in ("dense", "moe")}
+    y_host = {g: torch.empty(host[g]["h"].shape, dtype=torch.bfloat16, pin_memory=True)
+              for g in ("dense", "moe")}
     h2d = sum(v.numel() * v.element_size() for g in host.values() for v in g.values())
-    d2h = sum(v.numel() * v.element_size() for g in out_host.values() for v in g.values())
+    d2h = sum(2 * y.numel() * y.element_size() for y in y_host.values())   # h' and y
+
+    def host_step():
+        hd, hm = host["dense"], host["moe"]
+        snr.boundary_fused_host(hd["h"], hd["x"], hd["post_w"], hd["pre_w"], DENSE_N, EPS,
+                                y=y_host["dense"], stream=stream)
+        snr.moe_combine_boundary_host(hm["h"], hm["expert_out"], hm["topk_w"], hm["post_w"],
+                                      hm["pre_w"], MOE_N, EPS, y=y_host["moe"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            host_step()
+    torch.cuda.synchronize(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(device)
     torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            host_step()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, device)
+    snr.sync_status(stream)
+
+    # for comparison: copy the inputs in, run the device calls, copy h' and y out
+    out_host = {g: {k: torch.empty_like(host[g]["h"], device="cpu").pin_memory() for k in ("h", "y")}
+                for g in ("dense", "moe")}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(e2e_steps):
@@ -356,7 +456,7 @@ def bench_ours(args, rank, world, local_rank):
                     out_host[g][k].copy_(dev[g][k], non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize(device)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, device)
+    copy_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, device)
     snr.sync_status(stream)
 
     if rank != 0:
@@ -404,13 +504,19 @@ def bench_ours(args, rank, world, local_rank):
                      "frac": moe_gbs / peak, "traffic": traffic},
         "e2e": {"value": world * T_TOKENS / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms,
+                "path": "beam_boundary_fused_host + beam_moe_combine_boundary_host on page-locked "
+                        "host buffers: the kernels read the inputs and write h' and y over the "
+                        "CPU-GPU link",
+                "copy_then_compute": {"value": world * T_TOKENS / (copy_ms * 1e-3),
+                                      "ms_per_step": copy_ms}},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
     if not args.no_decode:
         line["config"]["decode"] = decode_latency(snr, device)
-        line["config"]["route_T16384_us"] = route_latency(snr, device)
+    if not args.no_next_rows:
+        line["config"]["next_rows"] = next_rows(snr, device, dev, peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -494,6 +600,8 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-size latency figures")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the timings of routing, Q/K norm and the NVFP4 boundaries")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
     if args.impl == "reference":

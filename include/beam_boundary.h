@@ -304,6 +304,31 @@ BEAM_API beam_status beam_moe_combine_boundary_nvfp4(beam_stream_t stream, uint1
                                             const beam_launch_opts* opts);
 
 /*
+ * The dense and MoE boundaries on a batch that lives in host memory. Any
+ * operand may be page-locked host memory (cudaHostAlloc, cudaHostRegister),
+ * device memory of the current device, or managed memory; pageable host memory
+ * only on a device that reads it through the host's page tables. The kernels
+ * read and write host operands directly over the CPU-GPU link: no staging
+ * copy and no device memory. On a Grace node that link is coherent NVLink-C2C,
+ * and the boundary runs at link speed with both directions busy at once.
+ * This is an addition of this library; the pages have no host-memory path.
+ * Results are bit-identical to beam_boundary_fused / beam_moe_combine_boundary.
+ * The launch uses the register kernels without L2 prefetch.
+ * Asynchronous on `stream`: touch no host operand until the stream is
+ * synchronised. Same arguments and errors as the device calls, checked before
+ * any CUDA call; then BEAM_ERR_ARG for an operand the device cannot address
+ * (pageable memory without pageable access, another device's memory).
+ */
+BEAM_API beam_status beam_boundary_fused_host(beam_stream_t stream, uint16_t* h, const uint16_t* x,
+                                     const uint16_t* post_w, const uint16_t* pre_w, int n,
+                                     float eps, int64_t T, int D, uint16_t* y_out);
+
+BEAM_API beam_status beam_moe_combine_boundary_host(beam_stream_t stream, uint16_t* h,
+                                           const uint16_t* expert_out, const float* topk_w,
+                                           const uint16_t* post_w, const uint16_t* pre_w, int n,
+                                           float eps, int64_t T, int D, uint16_t* y_out);
+
+/*
  * Synchronises `stream` and returns in *count the number of row sums (two per
  * row: the post-norm and the pre-norm sum) that took the exact integer path on
  * the current device since the last reset; reset != 0 zeroes the counter.

@@ -15,7 +15,8 @@ import ctypes
 from . import _lib
 from ._lib import LaunchOpts  # noqa: F401
 
-__all__ = ["boundary_fused", "moe_combine_boundary", "boundary_fused_nvfp4",
+__all__ = ["boundary_fused", "moe_combine_boundary", "boundary_fused_host",
+           "moe_combine_boundary_host", "boundary_fused_nvfp4",
            "moe_combine_boundary_nvfp4", "moe_route", "qk_norm", "sync_status",
            "exact_sum_count",
            "version", "BeamError", "LaunchOpts", "library"]
@@ -125,6 +126,77 @@ def moe_combine_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: floa
         lib.beam_moe_combine_boundary_ex(*args, _opts(opts))
     if st != 0:
         raise BeamError(st, "beam_moe_combine_boundary")
+    return y
+
+
+def _check_any(t, name: str, dtype, ndim: int):
+    """A CUDA tensor or a CPU tensor (page-locked, or pageable where the device
+    reads pageable memory: the library decides)."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type not in ("cuda", "cpu"):
+        raise ValueError(f"{name} must be a CUDA or CPU tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def _like_host(h):
+    import torch
+    if h.device.type == "cuda":
+        return torch.empty_like(h)
+    return torch.empty(h.shape, dtype=h.dtype, pin_memory=True)
+
+
+def boundary_fused_host(h, x, post_w, pre_w, n: int, eps: float = 1e-6, y=None, stream=None):
+    """Dense boundary on a batch in host memory: h, x, y (and the weights) may be
+    page-locked CPU tensors (``tensor.pin_memory()``), read and written by the kernels
+    over the CPU-GPU link. Asynchronous on ``stream`` (default: the current CUDA
+    stream): synchronise before touching the host tensors. Returns y (page-locked
+    CPU when h is on the CPU)."""
+    import torch
+    _check_any(h, "h", torch.bfloat16, 2)
+    _check_any(x, "x", torch.bfloat16, 2)
+    _check_any(post_w, "post_w", torch.bfloat16, 1)
+    _check_any(pre_w, "pre_w", torch.bfloat16, 1)
+    T, D = h.shape
+    if x.shape != h.shape or post_w.shape[0] != D or pre_w.shape[0] != D:
+        raise ValueError("shape mismatch: h, x [T, D]; post_w, pre_w [D]")
+    if y is None:
+        y = _like_host(h)
+    _check_any(y, "y", torch.bfloat16, 2)
+    st = _lib.load().beam_boundary_fused_host(_stream_ptr(stream), h.data_ptr(), x.data_ptr(),
+                                              post_w.data_ptr(), pre_w.data_ptr(), int(n),
+                                              float(eps), T, D, y.data_ptr())
+    if st != 0:
+        raise BeamError(st, "beam_boundary_fused_host")
+    return y
+
+
+def moe_combine_boundary_host(h, expert_out, topk_w, post_w, pre_w, n: int, eps: float = 1e-6,
+                              y=None, stream=None):
+    """MoE boundary on a batch in host memory (see ``boundary_fused_host``)."""
+    import torch
+    _check_any(h, "h", torch.bfloat16, 2)
+    _check_any(expert_out, "expert_out", torch.bfloat16, 3)
+    _check_any(topk_w, "topk_w", torch.float32, 2)
+    _check_any(post_w, "post_w", torch.bfloat16, 1)
+    _check_any(pre_w, "pre_w", torch.bfloat16, 1)
+    T, D = h.shape
+    K = _lib.BEAM_MOE_TOPK
+    if (expert_out.shape != (T, K, D) or topk_w.shape != (T, K) or post_w.shape[0] != D
+            or pre_w.shape[0] != D):
+        raise ValueError(f"shape mismatch: h [T, D]; expert_out [T, {K}, D]; topk_w [T, {K}]")
+    if y is None:
+        y = _like_host(h)
+    _check_any(y, "y", torch.bfloat16, 2)
+    st = _lib.load().beam_moe_combine_boundary_host(
+        _stream_ptr(stream), h.data_ptr(), expert_out.data_ptr(), topk_w.data_ptr(),
+        post_w.data_ptr(), pre_w.data_ptr(), int(n), float(eps), T, D, y.data_ptr())
+    if st != 0:
+        raise BeamError(st, "beam_moe_combine_boundary_host")
     return y
 
 

@@ -52,6 +52,9 @@ SIGNATURES = {
                                           _vp, _vp]),
     "beam_moe_combine_boundary_nvfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _i64, _i32,
                                                 _f32, _vp, _vp, _vp]),
+    "beam_boundary_fused_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _f32, _i64, _i32, _vp]),
+    "beam_moe_combine_boundary_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _i64, _i32,
+                                               _vp]),
     "beam_moe_route": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "beam_qk_norm": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _f32,
                              _i32]),

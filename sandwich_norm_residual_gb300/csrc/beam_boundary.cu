@@ -42,7 +42,10 @@ struct OccKey {
 struct DeviceInfo {
     bool checked = false;
     bool ok = false;
+    int ordinal = 0;
+    bool pageable_access = false;             // kernels may read pageable host memory
     int sms = 0;
+    long long l2_bytes = 0;
     int smem_optin = 0;                       // max dynamic + static shared memory per CTA
     KernelFn lim_fn[64] = {};                 // kernels whose dynamic smem limit was raised
     int lim_val[64] = {};
@@ -162,8 +165,10 @@ beam_status current_device(DeviceInfo** info) {
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceInfo& d = g_dev[dev];
     if (!d.checked) {
-        int major = 0, minor = 0, sms = 0, optin = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        int major = 0, minor = 0, sms = 0, optin = 0, pageable = 0, l2 = 0;
+        if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
@@ -171,6 +176,9 @@ beam_status current_device(DeviceInfo** info) {
             return BEAM_ERR_CUDA;
         }
         d.ok = (major == 10 && minor == 3);
+        d.ordinal = dev;
+        d.l2_bytes = l2;
+        d.pageable_access = pageable != 0;
         d.sms = sms;
         d.smem_optin = optin;
         d.checked = true;
@@ -309,10 +317,21 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
     const bool full_used = (kind == kDenseRing) ? full : (full && wbytes <= limit);
     const int smem = (kind == kDenseRing ? stages * slot_bytes : 0) + (full_used ? wbytes : 0);
 
+    const int prefetch = (opts && opts->prefetch_rows) ? (opts->prefetch_rows < 0 ? 0 : opts->prefetch_rows)
+                                                       : kAutoPrefetch;
     int per_sm = 0;
     st = resident_ctas(info, fn, nt, smem, &per_sm);
     if (st != BEAM_OK) return st;
-    if (opts && opts->ctas_per_sm) per_sm = opts->ctas_per_sm < per_sm ? opts->ctas_per_sm : per_sm;
+    if (opts && opts->ctas_per_sm) {
+        per_sm = opts->ctas_per_sm < per_sm ? opts->ctas_per_sm : per_sm;
+    } else if (kind != kDenseRing) {
+        // rows in flight (each CTA's current row and its prefetched ones) stay
+        // within half of L2; past that the prefetched rows are evicted before
+        // use (measured on the MoE rows: 3 CTAs/SM re-read 4% and ran 11% slower)
+        const long long row_in = moe ? (long long)D * 2 * (BEAM_MOE_TOPK + 1) + BEAM_MOE_TOPK * 4 : (long long)D * 4;
+        const long long fit = (info->l2_bytes / 2) / ((long long)info->sms * (prefetch + 1) * row_in);
+        if (fit < per_sm) per_sm = fit < 1 ? 1 : (int)fit;
+    }
     int64_t grid = (int64_t)per_sm * info->sms;
     if (grid > T) grid = T;
 
@@ -334,8 +353,7 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
     p.flags = 0u;
     if (opts && (opts->flags & BEAM_OPT_FORCE_EXACT_SUM)) p.flags |= beam::kFlagForceExact;
     if (opts && (opts->flags & BEAM_OPT_TEST_WAIT_TIMEOUT)) p.flags |= beam::kFlagTestWaitTimeout;
-    p.prefetch_rows = (opts && opts->prefetch_rows) ? (opts->prefetch_rows < 0 ? 0 : opts->prefetch_rows)
-                                                    : kAutoPrefetch;
+    p.prefetch_rows = prefetch;
     p.stages = stages;
     p.wait_ns = kWaitNs;
     p.test_wait_ns = kTestWaitNs;
@@ -371,13 +389,52 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
     return BEAM_OK;
 }
 
+// The address at which the current device's kernels reach `p`: device memory
+// of this device and managed memory as is, page-locked host memory at its
+// mapped device address, pageable host memory only where the device reads it
+// through the host's page tables.
+template <class P>
+beam_status device_address(const DeviceInfo* info, P*& p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return BEAM_ERR_CUDA;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+        return a.device == info->ordinal ? BEAM_OK : BEAM_ERR_ARG;
+    case cudaMemoryTypeManaged:
+        return BEAM_OK;
+    case cudaMemoryTypeHost:
+        if (!a.devicePointer) return BEAM_ERR_ARG;
+        p = static_cast<P*>(a.devicePointer);
+        return BEAM_OK;
+    default:
+        return info->pageable_access ? BEAM_OK : BEAM_ERR_ARG;
+    }
+}
+
+// Launch shape for operands in host memory: the register kernels, no L2
+// prefetch (the rows stream over the CPU-GPU link).
+const beam_launch_opts kHostOpts = {0u, 0, 0, -1, -1, {0, 0, 0}};
+
+template <class... P>
+beam_status host_addresses(P*&... ptrs) {
+    DeviceInfo* info = nullptr;
+    beam_status st = current_device(&info);
+    if (st != BEAM_OK) return st;
+    for (beam_status s : {device_address(info, ptrs)...})
+        if (s != BEAM_OK) return s;
+    return BEAM_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-beam_status beam_boundary_fused_ex(beam_stream_t stream, uint16_t* h, const uint16_t* x,
-                                   const uint16_t* post_w, const uint16_t* pre_w, int n, float eps,
-                                   int64_t T, int D, uint16_t* y_out, const beam_launch_opts* opts) {
+static beam_status dense_boundary(beam_stream_t stream, uint16_t* h, const uint16_t* x, const uint16_t* post_w,
+                                  const uint16_t* pre_w, int n, float eps, int64_t T, int D, uint16_t* y_out,
+                                  const beam_launch_opts* opts, bool host) {
     beam_status st = check_common(n, eps, T, D, opts);
     if (st != BEAM_OK || T == 0) return st;
     if (!h || !x || !post_w || !pre_w || !y_out) return BEAM_ERR_NULL;
@@ -389,7 +446,23 @@ beam_status beam_boundary_fused_ex(beam_stream_t stream, uint16_t* h, const uint
         return BEAM_ERR_ALIAS;
     if ((const void*)x != (const void*)h && overlaps(h, rows, x, rows)) return BEAM_ERR_ALIAS;
     if (overlaps(h, rows, post_w, vec) || overlaps(h, rows, pre_w, vec)) return BEAM_ERR_ALIAS;
+    if (host) {
+        st = host_addresses(h, x, post_w, pre_w, y_out);
+        if (st != BEAM_OK) return st;
+        opts = &kHostOpts;
+    }
     return launch(false, stream, h, x, nullptr, nullptr, post_w, pre_w, n, eps, T, D, y_out, opts);
+}
+
+beam_status beam_boundary_fused_ex(beam_stream_t stream, uint16_t* h, const uint16_t* x,
+                                   const uint16_t* post_w, const uint16_t* pre_w, int n, float eps,
+                                   int64_t T, int D, uint16_t* y_out, const beam_launch_opts* opts) {
+    return dense_boundary(stream, h, x, post_w, pre_w, n, eps, T, D, y_out, opts, false);
+}
+
+beam_status beam_boundary_fused_host(beam_stream_t stream, uint16_t* h, const uint16_t* x, const uint16_t* post_w,
+                                     const uint16_t* pre_w, int n, float eps, int64_t T, int D, uint16_t* y_out) {
+    return dense_boundary(stream, h, x, post_w, pre_w, n, eps, T, D, y_out, nullptr, true);
 }
 
 static beam_status check_nvfp4(int64_t T, int D, float gs, const uint8_t* q, const uint8_t* sf,
@@ -462,7 +535,7 @@ beam_status beam_boundary_fused(beam_stream_t stream, uint16_t* h, const uint16_
 static beam_status moe_boundary(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,
                                 const float* topk_w, float route_scale, const uint16_t* post_w,
                                 const uint16_t* pre_w, int n, float eps, int64_t T, int D, uint16_t* y_out,
-                                const beam_launch_opts* opts) {
+                                const beam_launch_opts* opts, bool host = false) {
     beam_status st = check_common(n, eps, T, D, opts);
     if (st != BEAM_OK || T == 0) return st;
     if (!std::isfinite(route_scale)) return BEAM_ERR_ARG;
@@ -479,8 +552,19 @@ static beam_status moe_boundary(beam_stream_t stream, uint16_t* h, const uint16_
     if (overlaps(h, rows, expert_out, erows) || overlaps(h, rows, topk_w, wbytes) || overlaps(h, rows, post_w, vec) ||
         overlaps(h, rows, pre_w, vec))
         return BEAM_ERR_ALIAS;
+    if (host) {
+        st = host_addresses(h, expert_out, topk_w, post_w, pre_w, y_out);
+        if (st != BEAM_OK) return st;
+        opts = &kHostOpts;
+    }
     return launch(true, stream, h, nullptr, expert_out, topk_w, post_w, pre_w, n, eps, T, D, y_out, opts,
                   route_scale);
+}
+
+beam_status beam_moe_combine_boundary_host(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,
+                                           const float* topk_w, const uint16_t* post_w, const uint16_t* pre_w,
+                                           int n, float eps, int64_t T, int D, uint16_t* y_out) {
+    return moe_boundary(stream, h, expert_out, topk_w, 1.0f, post_w, pre_w, n, eps, T, D, y_out, nullptr, true);
 }
 
 beam_status beam_moe_combine_boundary_ex(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,

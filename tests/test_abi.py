@@ -247,3 +247,25 @@ def test_nvfp4_argument_errors(lib):
     assert dense(opts=ctypes.byref(ring)) == _lib.BEAM_ERR_ARG     # the ring writes no NVFP4
     assert dense(opts=ctypes.byref(hook)) == _lib.BEAM_ERR_ARG
     assert moe(opts=ctypes.byref(_lib.LaunchOpts(reserved=(0, 1, 0)))) == _lib.BEAM_ERR_ARG
+
+
+def test_host_memory_calls_check_arguments_before_cuda(lib):
+    H, X, PW, QW, Y, E, W = (A + (i << 32) for i in range(7))
+
+    def dense(T=4, d=D, n=2, h=H, x=X, y=Y):
+        return lib.beam_boundary_fused_host(None, h, x, PW, QW, n, 1e-6, T, d, y)
+
+    def moe(T=4, d=D, h=H, e=E, w=W, y=Y):
+        return lib.beam_moe_combine_boundary_host(None, h, e, w, PW, QW, 2, 1e-6, T, d, y)
+
+    assert dense(d=12) == _lib.BEAM_ERR_SHAPE
+    assert dense(n=0) == _lib.BEAM_ERR_ARG
+    assert dense(T=0, h=None) == _lib.BEAM_OK
+    assert dense(y=None) == _lib.BEAM_ERR_NULL
+    assert moe(w=None) == _lib.BEAM_ERR_NULL
+    assert dense(x=X + 8) == _lib.BEAM_ERR_ALIGN
+    assert moe(e=E + 2) == _lib.BEAM_ERR_ALIGN
+    assert dense(y=H + 64) == _lib.BEAM_ERR_ALIAS
+    assert moe(h=E + 4096) == _lib.BEAM_ERR_ALIAS
+    # valid arguments reach CUDA: without a GPU that is a CUDA or device error
+    assert dense() in (_lib.BEAM_ERR_CUDA, _lib.BEAM_ERR_DEVICE)

@@ -699,3 +699,71 @@ def test_nvfp4_branch_is_the_stream_guard_bands_and_zero_tokens():
     h0 = torch.zeros((0, D), dtype=torch.bfloat16, device=DEV)
     q0, s0 = snr.boundary_fused_nvfp4(h0, h0, d["post_w"], d["pre_w"], 2, 1e-6, 336.0)
     assert q0.shape == (0, D // 2) and s0.shape == (0, D // 16)
+
+
+# --------------------------------------------------------------- batch in host memory
+
+def pinned(inp: dict) -> dict:
+    return {k: v.pin_memory() for k, v in inp.items()}
+
+
+def test_host_memory_dense_and_moe_full_match_the_oracle():
+    """Every operand page-locked in host memory: the kernels read and write it over
+    the CPU-GPU link; results equal the oracle and the device path bit for bit."""
+    cfg = CONFIGS[2]
+    inp = synth.dense_inputs(cfg)
+    hp = pinned(inp)
+    y = snr.boundary_fused_host(hp["h"], hp["x"], hp["post_w"], hp["pre_w"], cfg.n, cfg.eps)
+    snr.sync_status()
+    assert y.device.type == "cpu" and y.is_pinned()
+    want = oracle_dense(inp, cfg.n, cfg.eps)
+    check((bits(hp["h"]), bits(y)), want, f"{cfg.name} host memory")
+    cfg = CONFIGS[3]
+    m = synth.moe_inputs(cfg)
+    mp = pinned(m)
+    y = snr.moe_combine_boundary_host(mp["h"], mp["expert_out"], mp["topk_w"], mp["post_w"],
+                                      mp["pre_w"], cfg.n, cfg.eps)
+    snr.sync_status()
+    check((bits(mp["h"]), bits(y)), oracle_moe(m, cfg.n, cfg.eps), f"{cfg.name} host memory")
+
+
+def test_host_memory_mixed_with_device_operands_and_a_side_stream():
+    T, D = 300, 5120
+    inp = random_dense(T, D, seed=31)
+    want = oracle_dense(inp, 5, 1e-6)
+    hp = pinned(inp)
+    pw, qw = inp["post_w"].to(DEV), inp["pre_w"].to(DEV)
+    y_dev = torch.empty((T, D), dtype=torch.bfloat16, device=DEV)   # h on the host, y on the device
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        snr.boundary_fused_host(hp["h"], hp["x"], pw, qw, 5, 1e-6, y=y_dev, stream=s)
+    snr.sync_status(s)
+    check((bits(hp["h"]), bits(y_dev)), want, "host h and x, device weights and y")
+    cfg = CONFIGS[3]
+    m = synth.moe_inputs(cfg, rows=200)
+    wantm = oracle_moe(m, cfg.n, cfg.eps)
+    e_dev = m["expert_out"].to(DEV)                                  # expert rows already on the GPU
+    mp = pinned({k: v for k, v in m.items() if k != "expert_out"})
+    y = snr.moe_combine_boundary_host(mp["h"], e_dev, mp["topk_w"], mp["post_w"], mp["pre_w"],
+                                      cfg.n, cfg.eps)
+    snr.sync_status()
+    check((bits(mp["h"]), bits(y)), wantm, "host h, device expert rows")
+
+
+def test_host_memory_pageable_is_read_or_refused():
+    """Pageable memory works only where the device reads the host's page tables;
+    elsewhere the call refuses it with BEAM_ERR_ARG before launching."""
+    T, D = 8, 5120
+    inp = random_dense(T, D, seed=32)
+    want = oracle_dense(inp, 3, 1e-6)
+    h = inp["h"].clone()
+    y = torch.empty((T, D), dtype=torch.bfloat16)
+    try:
+        snr.boundary_fused_host(h, inp["x"], inp["post_w"], inp["pre_w"], 3, 1e-6, y=y)
+        snr.sync_status()
+    except snr.BeamError as e:
+        assert e.status == snr._lib.BEAM_ERR_ARG
+        assert torch.equal(h, inp["h"])      # nothing ran
+        print("pageable host memory refused (no pageable access on this device)")
+        return
+    check((bits(h), bits(y)), want, "pageable host memory")
