@@ -270,10 +270,10 @@ beam_status launch(bool moe, beam_stream_t stream, uint16_t* h, const uint16_t* 
     const int nt = threads_for(nvec, vpt);
     if (!nt) return BEAM_ERR_SHAPE;
 
-    // FULL: the row is exactly nt * vpt vectors; its kernels stage the FP32
-    // weights (8 D bytes) in shared memory
+    // FULL: the row is exactly nt * vpt vectors; its kernels stage the norm
+    // weights (4 D bytes, BF16) in shared memory
     const bool full = has_full(vpt) && nt * vpt == nvec;
-    const int wbytes = full ? 8 * D : 0;
+    const int wbytes = full ? 4 * D : 0;
     const int slot_bytes = 4 * D;
     int kind = moe ? kMoeRegs : kDenseRing;
     int stages = 0;

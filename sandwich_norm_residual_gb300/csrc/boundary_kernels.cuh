@@ -110,7 +110,8 @@ __device__ __forceinline__ void set_word(uint4& v, int q, uint32_t w) {
 // thread, and the certified result broadcast by warp 0.
 struct RedScratch {
     float2 part[kMaxThreads];
-    float2 result;  // (rounded sum, 1 if certified else 0)
+    float2 result;      // (rounded sum, 1 if certified else 0)
+    float inv_sf[128];  // NVFP4: RN32(y_global_scale / sf) for every E4M3 code sf, 0 for sf = 0
 };
 
 // Block-wide compensated sum of the squares of the row held in v[] (zeros in
@@ -200,6 +201,19 @@ __device__ __forceinline__ uint32_t f2_to_e2m1x2(float lo, float hi) {
     return r;
 }
 
+// RN32(a / 6) for a BF16 value a >= 0 (at most 8 significant bits) in three
+// operations instead of an IEEE division: t = RN32(a c) with c = RN32(1/6) is
+// within an ulp of a/6, so r = a - 6 t is exact in one FMA, and one correction
+// t + r c (Markstein's correction step for a known divisor) rounds correctly:
+// a/6 = (significand / 3) 2^k always lies at least 1/6 ulp from a rounding
+// midpoint, far beyond the correction's error. Checked for every non-negative
+// BF16 value in exact rational arithmetic.
+__device__ __forceinline__ float div6_bf16(float a) {
+    const float c = 0x1.555556p-3f;
+    const float t = __fmul_rn(a, c);
+    return __fmaf_rn(__fmaf_rn(-t, 6.0f, a), c, t);
+}
+
 // h is read and later overwritten by the same thread; this form also keeps
 // the read ahead of any later store (the NVFP4 MoE path parks x in the h row)
 __device__ __forceinline__ uint4 ld_stream_rw_ordered(const void* p) {
@@ -214,40 +228,25 @@ __device__ __forceinline__ float rms_factor(float S, int D, float eps) {
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
-// Norm weights as FP32 pairs, staged once per CTA in shared memory by FULL
-// kernels: ws[j] = post_w[j], ws[D + j] = pre_w[j]. Other kernels read the
-// BF16 weights from global memory (L1-cached) on every row.
-__device__ __forceinline__ void stage_weights(const BoundaryParams& p, float* ws) {
+// Norm weights staged once per CTA in shared memory by FULL kernels, as BF16
+// vectors (ws[vi] = post_w vector vi, ws[nvec + vi] = pre_w vector vi; one
+// 16-byte shared load per 8 weights, unpacked at use: measured faster than
+// FP32 copies, which need two loads). Other kernels read the BF16 weights from
+// global memory (L1-cached) on every row.
+__device__ __forceinline__ void stage_weights(const BoundaryParams& p, uint4* ws) {
     for (int vi = threadIdx.x; vi < p.nvec; vi += blockDim.x) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(p.post_w) + vi);
-        const uint4 b = __ldg(reinterpret_cast<const uint4*>(p.pre_w) + vi);
-        float4* dp = reinterpret_cast<float4*>(ws) + 2 * vi;
-        float4* dq = reinterpret_cast<float4*>(ws + p.D) + 2 * vi;
-        float2 a0 = bf2_to_f2(a.x), a1 = bf2_to_f2(a.y), a2 = bf2_to_f2(a.z), a3 = bf2_to_f2(a.w);
-        float2 b0 = bf2_to_f2(b.x), b1 = bf2_to_f2(b.y), b2 = bf2_to_f2(b.z), b3 = bf2_to_f2(b.w);
-        dp[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
-        dp[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
-        dq[0] = make_float4(b0.x, b0.y, b1.x, b1.y);
-        dq[1] = make_float4(b2.x, b2.y, b3.x, b3.y);
+        ws[vi] = __ldg(reinterpret_cast<const uint4*>(p.post_w) + vi);
+        ws[p.nvec + vi] = __ldg(reinterpret_cast<const uint4*>(p.pre_w) + vi);
     }
     __syncthreads();
 }
 
-// the 8 weights of vector vi as 4 FP32 pairs
+// the 8 weights of vector vi as 4 FP32 pairs, from shared memory (FULL) or global
 template <bool FULL>
-__device__ __forceinline__ void load_weights(const uint16_t* g, const float* ws, int vi, float2 (&w)[4]) {
-    if (FULL) {
-        const float4* p4 = reinterpret_cast<const float4*>(ws) + 2 * vi;
-        const float4 a = p4[0], b = p4[1];
-        w[0] = make_float2(a.x, a.y);
-        w[1] = make_float2(a.z, a.w);
-        w[2] = make_float2(b.x, b.y);
-        w[3] = make_float2(b.z, b.w);
-    } else {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(g) + vi);
+__device__ __forceinline__ void load_weights(const uint16_t* g, const uint4* ws, int vi, float2 (&w)[4]) {
+    const uint4 v = FULL ? ws[vi] : __ldg(reinterpret_cast<const uint4*>(g) + vi);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) w[q] = bf2_to_f2(word(v, q));
-    }
+    for (int q = 0; q < 4; ++q) w[q] = bf2_to_f2(word(v, q));
 }
 
 // Everything after the branch x and the stream h of a row are in registers:
@@ -258,7 +257,7 @@ __device__ __forceinline__ void load_weights(const uint16_t* g, const float* ws,
 template <int VPT, bool MOE, bool FULL, bool QUANT, class AfterS1>
 __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long row, uint4 (&xv)[VPT],
                                            uint4 (&hv)[VPT], RedScratch* rs, ExactScratch* sc,
-                                           const float* ws, AfterS1 after_s1) {
+                                           const uint4* ws, AfterS1 after_s1) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const bool force_exact = (p.flags & kFlagForceExact) != 0;
     const size_t base = (size_t)row * (size_t)p.D;
@@ -340,7 +339,7 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
         uint4 yv = make_uint4(0, 0, 0, 0);
         if (valid) {
             float2 qw[4];
-            load_weights<FULL>(p.pre_w, ws ? ws + p.D : nullptr, vi, qw);
+            load_weights<FULL>(p.pre_w, ws ? ws + p.nvec : nullptr, vi, qw);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 set_word(yv, q, f2_to_bf2(mul2_rn(mul2_rn(bf2_to_f2(word(hv[i], q)), r2v), qw[q])));
@@ -355,15 +354,15 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
                 am = fmaxf(am, fmaxf(fabsf(f.x), fabsf(f.y)));
             }
             am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-            const uint32_t sfb = f32_to_e4m3(__fmul_rn(__fdiv_rn(am, 6.0f), p.y_gs));
-            const float sfv = e4m3_to_f32(sfb);
+            const uint32_t sfb = f32_to_e4m3(__fmul_rn(div6_bf16(am), p.y_gs));
             uint32_t codes = 0u;
-            if (sfv != 0.0f) {
-                const float inv = __fdiv_rn(p.y_gs, sfv);
+            if (sfb != 0u) {  // code 0 is the only zero scale (the argument is >= 0)
+                const float inv = rs->inv_sf[sfb & 0x7Fu];
+                const float2 iv = make_float2(inv, inv);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float2 f = bf2_to_f2(word(yv, q));
-                    codes |= f2_to_e2m1x2(__fmul_rn(f.x, inv), __fmul_rn(f.y, inv)) << (8 * q);
+                    const float2 f = mul2_rn(bf2_to_f2(word(yv, q)), iv);
+                    codes |= f2_to_e2m1x2(f.x, f.y) << (8 * q);
                 }
             }
             if (valid) {
@@ -382,16 +381,23 @@ struct NoOp {
 // L2 for the inputs of this CTA's row `prefetch_rows` ahead.
 template <int VPT, bool MOE, bool FULL, bool QUANT>
 __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryParams p) {
-    extern __shared__ __align__(16) float ws_dyn[];
+    extern __shared__ __align__(16) uint4 ws_dyn[];
     __shared__ RedScratch rs;
     __shared__ ExactScratch sc;
     const int tid = threadIdx.x, nt = blockDim.x;
-    const float* ws = FULL ? ws_dyn : nullptr;
+    const uint4* ws = FULL ? ws_dyn : nullptr;
 
     // prologue that reads only the norm weights; with a programmatic launch it
     // overlaps the previous kernel on the stream (the caller guarantees that
     // kernel does not write the weights)
     pdl_trigger();
+    if (QUANT) {
+        // inverse block scales, read after the first row reduction's barrier
+        for (int i = tid; i < 128; i += nt) {
+            const float sf = e4m3_to_f32((uint32_t)i);
+            rs.inv_sf[i] = sf != 0.0f ? __fdiv_rn(p.y_gs, sf) : 0.0f;
+        }
+    }
     if (FULL) stage_weights(p, ws_dyn);
     pdl_wait();
     if (tid == 0)
@@ -457,7 +463,7 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
 // mbarrier. One thread refills a slot with the row `stages` ahead as soon as
 // the post-norm reduction's barrier shows every thread has read it, so up to
 // stages-1 rows per CTA are in flight while a row is computed. FULL kernels
-// keep the FP32 weights after the ring.
+// keep the BF16 weights after the ring.
 template <int VPT, bool FULL>
 __global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const BoundaryParams p) {
     extern __shared__ __align__(128) unsigned char ring[];
@@ -470,7 +476,7 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const Bounda
     const uint32_t row_bytes = (uint32_t)p.D * 2u;
     const long long G = gridDim.x;
     const long long n_iter = (p.T - blockIdx.x + G - 1) / G;  // grid <= T: at least one row
-    float* ws = FULL ? reinterpret_cast<float*>(ring + (size_t)S * 2u * row_bytes) : nullptr;
+    uint4* ws = FULL ? reinterpret_cast<uint4*>(ring + (size_t)S * 2u * row_bytes) : nullptr;
 
     auto slot_x = [&](int s) { return ring + (size_t)s * 2u * row_bytes; };
     auto issue = [&](long long i) {  // thread 0 only
