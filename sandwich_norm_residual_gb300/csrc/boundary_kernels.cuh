@@ -84,10 +84,6 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16)
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
-}
 
 // One thread asks L2 for the inputs of row r (branch rows and h)
 template <bool MOE>

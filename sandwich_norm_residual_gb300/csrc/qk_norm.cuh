@@ -12,9 +12,11 @@
 //          queries (correctly rounded, see ssmax_scale); keys keep vn.
 //
 // One warp per token walks its heads: each pass takes 4 heads, one per group
-// of 8 lanes, and lane i of a group holds elements 16i .. 16i+15 of its head,
-// so the RoPE partner of a lane is lane ^ 4 and the row sums merge over 3
-// shuffle levels. Two batches of 8 heads are in flight at a time.
+// of 8 lanes, and lane i of a group holds elements 8i .. 8i+7 and 64+8i ..
+// 64+8i+7 of its head: both halves of every rotate-half pair are in the same
+// lane, which keeps the 8 cos and 8 sin values it needs in registers for the
+// whole token. The row sums merge over 3 shuffle levels. Two batches of 8 heads
+// are in flight at a time.
 #pragma once
 
 #include "row_sum.cuh"
@@ -129,7 +131,6 @@ __global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
         return;
     }
     const int nh = p.nq + p.nk;
-    const bool upper = li >= 4;  // holds elements j + 64 of the rotate-half pairs
 
     // ---- loads of one batch: pass b takes head h0 + 4b + grp
     auto row_of = [&](int hh) -> uint16_t* {
@@ -141,9 +142,9 @@ __global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
         for (int b = 0; b < 2; ++b) {
             const int hh = h0 + 4 * b + grp;
             if (hh < nh) {
-                const uint4* r = reinterpret_cast<const uint4*>(row_of(hh) + 16 * li);
-                v[b][0] = r[0];
-                v[b][1] = r[1];
+                const uint4* r = reinterpret_cast<const uint4*>(row_of(hh) + 8 * li);
+                v[b][0] = r[0];  // elements 8 li ..
+                v[b][1] = r[8];  // elements 64 + 8 li ..
             } else {
                 v[b][0] = v[b][1] = make_uint4(0, 0, 0, 0);
             }
@@ -153,12 +154,19 @@ __global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
     load(va, 0);
 
     // ---- per-lane constants: weights and cos/sin (RoPE) or the query scale (SSMax)
-    const uint4* qwp = reinterpret_cast<const uint4*>(p.qw + 16 * li);
-    const uint4* kwp = reinterpret_cast<const uint4*>(p.kw + 16 * li);
-    const uint4 qw0 = __ldg(qwp), qw1 = __ldg(qwp + 1), kw0 = __ldg(kwp), kw1 = __ldg(kwp + 1);
-    // cos | sin of this lane's 16 pairs (RoPE), re-read per head from L1
-    const float4* cs = p.mode == 0
-        ? reinterpret_cast<const float4*>(p.table + pos * kQKHeadDim + 16 * (li & 3)) : nullptr;
+    const uint4* qwp = reinterpret_cast<const uint4*>(p.qw + 8 * li);
+    const uint4* kwp = reinterpret_cast<const uint4*>(p.kw + 8 * li);
+    const uint4 qw0 = __ldg(qwp), qw1 = __ldg(qwp + 8), kw0 = __ldg(kwp), kw1 = __ldg(kwp + 8);
+    // cos and sin of this lane's 8 pairs (RoPE), for every head of the token
+    float2 cv[4], sv[4];
+    if (p.mode == 0) {
+        const float4* cs = reinterpret_cast<const float4*>(p.table + pos * kQKHeadDim + 8 * li);
+        const float4 c0 = __ldg(cs), c1 = __ldg(cs + 1), s0 = __ldg(cs + 16), s1 = __ldg(cs + 17);
+        cv[0] = make_float2(c0.x, c0.y); cv[1] = make_float2(c0.z, c0.w);
+        cv[2] = make_float2(c1.x, c1.y); cv[3] = make_float2(c1.z, c1.w);
+        sv[0] = make_float2(s0.x, s0.y); sv[1] = make_float2(s0.z, s0.w);
+        sv[2] = make_float2(s1.x, s1.y); sv[3] = make_float2(s1.z, s1.w);
+    }
     const float g = p.mode != 0 ? ssmax_scale(pos, lane) : 1.0f;
 
     auto process = [&](const uint4 (&v)[2][2], int h0) {
@@ -191,7 +199,8 @@ __global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
                     if (li == 0 && live) atomicAdd(&g_exact_sum_count, 1ull);
                 }
             }
-            const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(Sr, 128.0f), p.eps)));
+            // Sr / 128 as an exact scaling by 2^-7 (the same rounding of the same value)
+            const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(Sr, 0x1p-7f), p.eps)));
             const float2 rv = make_float2(r, r);
             const uint4 w0 = is_q ? qw0 : kw0, w1 = is_q ? qw1 : kw1;
             const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -199,18 +208,18 @@ __global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) n[i] = f2_to_bf2(mul2_rn(mul2_rn(bf2_to_f2(w[i]), rv), bf2_to_f2(ww[i])));
             if (p.mode == 0) {
+                // words i (elements j) and i + 4 (elements j + 64) form the pairs.
+                // The products are packed; the sums are scalar __fadd_rn /
+                // __fsub_rn, which never merge into an FMA (a packed add whose
+                // only operand is a packed product was measured to fuse into an
+                // FMA despite its explicit rounding modifier).
 #pragma unroll
-                for (int i = 0; i < 8; i += 2) {
-                    const float4 cc = __ldg(cs + i / 2), ss = __ldg(cs + 16 + i / 2);
-                    const float2 ci[2] = {make_float2(cc.x, cc.y), make_float2(cc.z, cc.w)};
-                    const float2 si[2] = {make_float2(ss.x, ss.y), make_float2(ss.z, ss.w)};
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint32_t m = __shfl_xor_sync(full, n[i + u], 4);
-                        const float2 pa = mul2_rn(bf2_to_f2(n[i + u]), ci[u]);
-                        const float2 pb = mul2_rn(bf2_to_f2(m), si[u]);
-                        o[i + u] = f2_to_bf2(upper ? add2_rn(pa, pb) : sub2_rn(pa, pb));
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    const float2 a = bf2_to_f2(n[i]), b = bf2_to_f2(n[i + 4]);
+                    const float2 ac = mul2_rn(a, cv[i]), bs = mul2_rn(b, sv[i]);
+                    const float2 bc = mul2_rn(b, cv[i]), as = mul2_rn(a, sv[i]);
+                    o[i] = f2_to_bf2(make_float2(__fsub_rn(ac.x, bs.x), __fsub_rn(ac.y, bs.y)));
+                    o[i + 4] = f2_to_bf2(make_float2(__fadd_rn(bc.x, as.x), __fadd_rn(bc.y, as.y)));
                 }
             } else if (is_q) {
                 const float2 gv = make_float2(g, g);
@@ -221,9 +230,9 @@ __global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
                 for (int i = 0; i < 8; ++i) o[i] = n[i];
             }
             if (live) {
-                uint4* dst = reinterpret_cast<uint4*>(row_of(hh) + 16 * li);
+                uint4* dst = reinterpret_cast<uint4*>(row_of(hh) + 8 * li);
                 dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                dst[8] = make_uint4(o[4], o[5], o[6], o[7]);
             }
         }
     };

@@ -10,6 +10,11 @@
 
 namespace beam {
 
+// bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16)
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
 __device__ unsigned int g_status_word;  // bit 0: a bounded wait gave up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
