@@ -131,6 +131,12 @@ __global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
         return;
     }
     const int nh = p.nq + p.nk;
+    // ask L2 for the token's whole q and k rows now, so that DRAM streams all
+    // its heads while the batches below are loaded and processed
+    if (lane == 0) {
+        if (p.nq) prefetch_l2(p.q + (size_t)t * p.nq * kQKHeadDim, (uint32_t)p.nq * kQKHeadDim * 2u);
+        if (p.nk) prefetch_l2(p.k + (size_t)t * p.nk * kQKHeadDim, (uint32_t)p.nk * kQKHeadDim * 2u);
+    }
 
     // ---- loads of one batch: pass b takes head h0 + 4b + grp
     auto row_of = [&](int hh) -> uint16_t* {
