@@ -12,7 +12,9 @@
 //   w_k = (s_k / sum_k s_k) * scale, the sum taken in output order
 //
 // One warp per token; lane l holds experts 8l .. 8l+7 (256 experts), so a group
-// of 256/n_group experts spans 32/n_group neighbouring lanes.
+// of 256/n_group experts spans 32/n_group neighbouring lanes. Each top-k round
+// is two warp reductions: the largest biased score (as an order-preserving
+// unsigned key), then the lowest expert index holding it.
 #pragma once
 
 #include <cstdint>
@@ -37,6 +39,13 @@ __device__ __forceinline__ bool ranks_before(float v1, int i1, float v2, int i2)
     return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
+// unsigned key that orders like the float (never 0 for a non-NaN value; -0 and
+// +0 differ, but a biased score s + bias is never -0 since s is never -0)
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
     const int lane = threadIdx.x & 31;
     const long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -51,7 +60,7 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
     float s[8], b[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        s[i] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z[i])));
+        s[i] = __frcp_rn(__fadd_rn(1.0f, expf(-z[i])));  // RN(1 / (1 + e)), as a division
         b[i] = __fadd_rn(s[i], bias[i]);
     }
 
@@ -89,29 +98,41 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
     }
     const bool eligible = rank < p.topk_group;
 
-    // ---- topk best biased scores among eligible experts, one warp argmax each
-    unsigned taken = eligible ? 0u : 0xFFu;  // bit i: expert 8 lane + i unavailable
-    float sel_s[kRouteMaxTopk];
+    // ---- topk best biased scores among eligible experts: per round, the best
+    // key of each lane (lowest local index among equal keys), the warp's
+    // largest key, then the lowest expert index that holds it
+    uint32_t key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) key[i] = eligible ? order_key(b[i]) : 0u;  // 0: unavailable
     int sel_i[kRouteMaxTopk];
 #pragma unroll
     for (int k = 0; k < kRouteMaxTopk; ++k) {
         if (k >= p.topk) break;
-        float bv = -INFINITY, sv = 0.0f;
-        int bi = 0x7FFFFFFF;
+        uint32_t lk = 0u;
+        int li = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = 8 * lane + i;
-            if (!((taken >> i) & 1u) && ranks_before(b[i], e, bv, bi)) { bv = b[i]; bi = e; sv = s[i]; }
-        }
+        for (int i = 0; i < 8; ++i)
+            if (key[i] > lk) { lk = key[i]; li = i; }
+        const uint32_t m = __reduce_max_sync(full, lk);
+        const uint32_t e = __reduce_min_sync(full, (lk == m) ? (uint32_t)(8 * lane + li) : 0xFFFFFFFFu);
+        if ((int)(e >> 3) == lane) {
 #pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            const float ov = __shfl_xor_sync(full, bv, off), os = __shfl_xor_sync(full, sv, off);
-            const int oi = __shfl_xor_sync(full, bi, off);
-            if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; sv = os; }
+            for (int i = 0; i < 8; ++i)
+                if (i == (int)(e & 7u)) key[i] = 0u;
         }
-        if ((bi >> 3) == lane) taken |= 1u << (bi & 7);
-        sel_s[k] = sv;
-        sel_i[k] = bi;
+        sel_i[k] = (int)e;
+    }
+    // the unbiased score of each pick, from the lane that holds it
+    float sel_s[kRouteMaxTopk];
+#pragma unroll
+    for (int k = 0; k < kRouteMaxTopk; ++k) {
+        if (k >= p.topk) break;
+        const int e = sel_i[k];
+        float mine = s[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
+            if (i == (e & 7)) mine = s[i];
+        sel_s[k] = __shfl_sync(full, mine, e >> 3);
     }
 
     // ---- weights: unbiased scores, renormalised in output order, scaled
