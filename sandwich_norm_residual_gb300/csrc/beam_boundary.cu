@@ -663,7 +663,7 @@ beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k, cons
     p.nq = n_q_heads;
     p.nk = n_kv_heads;
     p.eps = eps;
-    p.errk = error_factor_terms(8.0, 1 + 3);  // 8 terms per FP32 lane, lane merge + 3 shuffle levels
+    p.errk = error_factor_terms(8.0, 2 + 2);  // 8 terms per FP32 lane, 2 merges in the lane + 2 shuffle levels
     p.mode = mode;
     p.flags = (flags & BEAM_OPT_FORCE_EXACT_SUM) ? beam::kFlagForceExact : 0u;
     const int64_t blocks = (T + 7) / 8;  // 8 warps, one token each
