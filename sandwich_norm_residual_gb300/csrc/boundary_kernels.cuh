@@ -106,21 +106,28 @@ __device__ __forceinline__ void set_word(uint4& v, int q, uint32_t w) {
 // thread, and the certified result broadcast by warp 0.
 struct RedScratch {
     float2 part[kMaxThreads];
-    float2 result;      // (rounded sum, 1 if certified else 0)
+    float4 result;      // (rounded sum, 1 if certified else 0, its RMS factor, unused)
     float inv_sf[128];  // NVFP4: RN32(y_global_scale / sf) for every E4M3 code sf, 0 for sf = 0
 };
+
+// r = 1 / sqrt(S/D + eps), each operation rounded to nearest
+__device__ __forceinline__ float rms_factor(float S, int D, float eps) {
+    float ms = __fdiv_rn(S, (float)D);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
 
 // Block-wide compensated sum of the squares of the row held in v[] (zeros in
 // unused slots). Every thread folds its two FP32 lanes into one pair and
 // stores it; warp 0 merges the pairs (lane l takes l, l+32, ... in order, then
 // a 5-level xor butterfly), certifies the rounding and broadcasts it. The
 // other warps run `overlap` while warp 0 merges; warp 0 runs it afterwards.
-// Returns true with *out = RN32(exact sum) when certified; false when the
-// exact path must decide. The first barrier also orders every store this
+// Returns true with *out = RN32(exact sum) and *out_r = rms_factor(*out, D,
+// eps) (formed once, by thread 0) when certified; false when the exact path
+// must decide. The first barrier also orders every store this
 // block issued before the call ahead of any load after it.
 template <int VPT, class Overlap>
-__device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float errk, RedScratch* rs,
-                                                  float* out, Overlap overlap) {
+__device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float errk, int D, float eps,
+                                                  RedScratch* rs, float* out, float* out_r, Overlap overlap) {
     float2 s = make_float2(0.f, 0.f), c = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
@@ -152,15 +159,17 @@ __device__ __forceinline__ bool block_sum_squares(const uint4 (&v)[VPT], float e
         if (threadIdx.x == 0) {
             float r;
             bool ok = certify_round(S, C, errk, &r);
-            rs->result = make_float2(r, ok ? 1.0f : 0.0f);
+            // one thread forms the RMS factor of a certified sum for the block
+            rs->result = make_float4(r, ok ? 1.0f : 0.0f, ok ? rms_factor(r, D, eps) : 0.0f, 0.0f);
         }
     } else {
         overlap();
     }
     __syncthreads();
     if (merger) overlap();
-    const float2 res = rs->result;
+    const float4 res = rs->result;
     *out = res.x;
+    *out_r = res.z;
     return res.y != 0.0f;
 }
 
@@ -219,11 +228,6 @@ __device__ __forceinline__ uint4 ld_stream_rw_ordered(const void* p) {
     return r;
 }
 
-__device__ __forceinline__ float rms_factor(float S, int D, float eps) {
-    float ms = __fdiv_rn(S, (float)D);
-    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-}
-
 // Norm weights staged once per CTA in shared memory by FULL kernels, as BF16
 // vectors (ws[vi] = post_w vector vi, ws[nvec + vi] = pre_w vector vi; one
 // 16-byte shared load per 8 weights, unpacked at use: measured faster than
@@ -268,8 +272,8 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
             for (int q = 0; q < 4; ++q)
                 set_word(hv[i], q, f2_to_bf2(mul2_rn(c1, bf2_to_f2(word(hv[i], q)))));
     };
-    float S1;
-    const bool ok1 = block_sum_squares<VPT>(xv, p.errk, rs, &S1, scale_stream);
+    float S1, r1;
+    const bool ok1 = block_sum_squares<VPT>(xv, p.errk, p.D, p.eps, rs, &S1, &r1, scale_stream);
     after_s1();
     if (!ok1 || force_exact) {
         // the exact path reads x from global memory: the input row (dense)
@@ -288,8 +292,8 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
             srow = park;
         }
         S1 = exact_row_sum_squares(srow, p.D, sc);
+        r1 = rms_factor(S1, p.D, p.eps);
     }
-    const float r1 = rms_factor(S1, p.D, p.eps);
     const float2 r1v = make_float2(r1, r1);
 
     // ---- xn, b = bf16(c2 xn), h' = a + b (in registers)
@@ -319,12 +323,12 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
             if (FULL || vi < p.nvec) st_stream(p.h + base + (size_t)vi * 8, hv[i]);
         }
     };
-    float S2;
-    if (!block_sum_squares<VPT>(hv, p.errk, rs, &S2, store_stream) || force_exact) {
+    float S2, r2;
+    if (!block_sum_squares<VPT>(hv, p.errk, p.D, p.eps, rs, &S2, &r2, store_stream) || force_exact) {
         __syncthreads();  // warp 0 stored its part of h' after the reduction's last barrier
         S2 = exact_row_sum_squares(p.h + base, p.D, sc);
+        r2 = rms_factor(S2, p.D, p.eps);
     }
-    const float r2 = rms_factor(S2, p.D, p.eps);
     const float2 r2v = make_float2(r2, r2);
 
     // ---- y = bf16((h' r2) pre_w), stored as BF16 or quantised to NVFP4
