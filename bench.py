@@ -348,6 +348,36 @@ def next_rows(snr, device, dev, peak: float) -> dict:
     return out
 
 
+def moe_stress(snr, device, peak: float, reps: int = 5) -> dict:
+    """The MoE stress workload at full size: T = 131072 tokens, n = 104, Student-t(3)
+    expert rows with 0.1% of them x100, one launch of 14.8 GB of algorithmic traffic.
+    Inputs are generated in chunks straight into device memory."""
+    import torch
+    import synth
+    from synth import CONFIGS
+    cfg = CONFIGS[4]
+    T, D, K = cfg.T, cfg.D, cfg.K
+    e = torch.empty((T, K, D), dtype=torch.bfloat16, device=device)
+    for r in range(0, T, 8192):
+        e[r:r + 8192].copy_(synth.expert_rows(cfg, r, min(8192, T - r)))
+    h = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["h"], T * D).reshape(T, D)).to(device)
+    w = torch.from_numpy(synth.topk_weights(cfg.seed, synth.STREAMS["topk"], T, K,
+                                            cfg.route_scale)).to(device)
+    pw = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["post_w"], D, 0, 0.1, 1.0)).to(device)
+    qw = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["pre_w"], D, 0, 0.1, 1.0)).to(device)
+    y = torch.empty_like(h)
+    stream = torch.cuda.Stream(device)
+    us = _time_launches(lambda i: snr.moe_combine_boundary(h, e, w, pw, qw, cfg.n, cfg.eps, y=y,
+                                                           stream=stream), stream, reps, warmup=2)
+    snr.sync_status(stream)
+    nbytes = T * (22 * D + 32) + 4 * D
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del e, h, w, y
+    torch.cuda.empty_cache()
+    return {"T": T, "n": cfg.n, "us": round(us, 1), "bytes": nbytes, "GBps": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4), "tokens_per_s": T / (us * 1e-6)}
+
+
 def bench_ours(args, rank, world, local_rank):
     import torch
     import sandwich_norm_residual_gb300 as snr
@@ -517,6 +547,8 @@ def bench_ours(args, rank, world, local_rank):
         line["config"]["decode"] = decode_latency(snr, device)
     if not args.no_next_rows:
         line["config"]["next_rows"] = next_rows(snr, device, dev, peak)
+    if not args.no_stress:
+        line["config"]["moe_stress_T131072"] = moe_stress(snr, device, peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -600,6 +632,8 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-size latency figures")
+    ap.add_argument("--no-stress", action="store_true",
+                    help="skip the T = 131072 MoE stress timing")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the timings of routing, Q/K norm and the NVFP4 boundaries")
     args = ap.parse_args(argv)

@@ -135,17 +135,20 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
         sel_s[k] = __shfl_sync(full, mine, e >> 3);
     }
 
-    // ---- weights: unbiased scores, renormalised in output order, scaled
+    // ---- weights: unbiased scores, renormalised in output order, scaled; lane
+    // k < topk writes output k (one division per lane)
     float sum = sel_s[0];
 #pragma unroll
     for (int k = 1; k < kRouteMaxTopk; ++k)
         if (k < p.topk) sum = __fadd_rn(sum, sel_s[k]);
+    float my_s = sel_s[0];
+    int my_i = sel_i[0];
 #pragma unroll
-    for (int k = 0; k < kRouteMaxTopk; ++k) {
-        if (k < p.topk && lane == k) {
-            p.idx[t * p.topk + k] = sel_i[k];
-            p.w[t * p.topk + k] = __fmul_rn(__fdiv_rn(sel_s[k], sum), p.scale);
-        }
+    for (int k = 1; k < kRouteMaxTopk; ++k)
+        if (k < p.topk && lane == k) { my_s = sel_s[k]; my_i = sel_i[k]; }
+    if (lane < p.topk) {
+        p.idx[t * p.topk + lane] = my_i;
+        p.w[t * p.topk + lane] = __fmul_rn(__fdiv_rn(my_s, sum), p.scale);
     }
 }
 
