@@ -36,9 +36,9 @@ METRIC = "fused boundary tokens/s at T=16384 (dense + MoE boundary of one decode
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "moe": {"bytes_per_launch": 1_517_332_000 + 292_803_328, "source_sha": "5fd6866f1991b313",
+    "moe": {"bytes_per_launch": 1_515_679_000 + 292_293_632, "source_sha": "7d1bdac54714bd13",
             "profile": "profiles/moe_combine_boundary_T16384.md"},
-    "dense": {"bytes_per_launch": 335_723_000 + 274_742_784, "source_sha": "5fd6866f1991b313",
+    "dense": {"bytes_per_launch": 335_686_000 + 274_988_032, "source_sha": "7d1bdac54714bd13",
               "profile": "profiles/dense_boundary_T16384.md"},
 }
 
