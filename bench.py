@@ -571,25 +571,38 @@ def oracle_step_sample(rows: int, row0: int = 0):
             synth.moe_inputs(CONFIGS[3], row_start=row0, rows=rows))
 
 
-def oracle_step(dn, mo):
+def oracle_step(dn, mo, threads: int = 1):
     import oracle
-    oracle.boundary(dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, threads=1)
+    oracle.boundary(dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, threads=threads)
     oracle.moe_boundary(mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"], mo["pre_w"], MOE_N,
-                        EPS, threads=1)
+                        EPS, threads=threads)
 
 
-def cpu_baseline(seconds: float) -> dict:
-    """The oracle, as it stands, on one host core, over a bounded sample of the workload."""
-    rows, done, spent = 16, 0, 0.0
+def _oracle_rate(seconds: float, threads: int) -> tuple[float, int, float]:
+    rows, done, spent = 16 * threads, 0, 0.0
     while spent < seconds:
         dn, mo = oracle_step_sample(rows, done % T_TOKENS)
         t0 = time.perf_counter()
-        oracle_step(dn, mo)
+        oracle_step(dn, mo, threads)
         spent += time.perf_counter() - t0
         done += rows
-    return {"value": done / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    return done / spent, done, spent
+
+
+def cpu_baseline(seconds: float) -> dict:
+    """The oracle, as it stands, on one host core, over a bounded sample of the workload;
+    beside it the same oracle row-parallel on every host core."""
+    rate, done, spent = _oracle_rate(seconds, 1)
+    line = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{done} of the {T_TOKENS} tokens through both boundaries, "
                       f"{spent:.1f} s single-threaded C"}
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    if cores > 1:
+        rate_n, done_n, spent_n = _oracle_rate(seconds / 2, cores)
+        line["all_cores"] = {"value": rate_n, "unit": "tokens/s", "cores": cores,
+                             "sample": f"{done_n} tokens, {spent_n:.1f} s, rows split over {cores} "
+                                       "threads"}
+    return line
 
 
 def bench_reference(args, rank, world):
