@@ -32,6 +32,8 @@ DENSE_N, MOE_N, EPS = 7, 20, 1e-6
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "fused boundary tokens/s at T=16384 (dense + MoE boundary of one decoder layer)"
+WORKLOAD = (f"layer boundary pair, T={T_TOKENS} tokens per GPU, D={D}: dense boundary n={DENSE_N} + "
+            f"MoE top-8 combine boundary n={MOE_N}, eps=1e-6; storage bf16, math fp32")
 
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only for the kernel source it was taken on.
@@ -515,9 +517,7 @@ def bench_ours(args, rank, world, local_rank):
         "dtype": "f32",
         "data": "synthetic",
         "config": {
-            "workload": f"layer boundary pair, T={T_TOKENS} tokens per GPU, D={D}: dense "
-                        f"boundary n={DENSE_N} + MoE top-8 combine boundary n={MOE_N}, eps=1e-6; "
-                        "storage bf16, math fp32",
+            "workload": WORKLOAD,
             "T": T_TOKENS, "D": D,
             "l2": "inputs larger than L2 (129 MB): no flush between steps",
             "dense": {"us": dense_us, "tokens_per_s": T_TOKENS / (dense_us * 1e-6),
@@ -623,9 +623,8 @@ def bench_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spent / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"layer boundary pair, T={T_TOKENS}, D={D}: dense n={DENSE_N} + "
-                               f"MoE n={MOE_N}; each step a {rows}-token sample",
-                   "T": T_TOKENS, "D": D},
+        "config": {"workload": WORKLOAD, "T": T_TOKENS, "D": D,
+                   "sample": f"each step runs {rows} of the workload's tokens through both boundaries"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"{rows} tokens per step, {args.steps} steps"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
