@@ -192,7 +192,8 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
     """Decode-size boundaries, launch-bound: CUDA-graph replays, with and without
     programmatic dependent launch (PDL). T = 4: microseconds per boundary over
     200 captured calls. T = 64: microseconds per 104-boundary chain (n = 2..105,
-    fresh x and weights per boundary)."""
+    fresh x and weights per boundary), of dense boundaries only and of dense and
+    MoE boundaries in turn as a decoder's 52 layers run them."""
     import torch
     import synth
     from synth import CONFIGS
@@ -238,7 +239,22 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
                 snr.boundary_fused(h1, d["x"], d["post_w"], d["pre_w"], c1.n + s, c1.eps, y=ys[s],
                                    opts=pdl_opts[pdl], stream=stream)
         out[f"chain104_T64_us{'_pdl' if pdl else ''}"] = timed_graph(body1, "chain", replays)
-    # the same chain launched one call at a time, no graph
+    # the chain as a decoder runs it: attention (dense) and MoE boundaries in turn
+    from synth import layer_chain_inputs
+    _, lsteps = layer_chain_inputs(c1, CONFIGS[3])
+    lsteps = [{k: (v.to(device) if k != "kind" else v) for k, v in st.items()} for st in lsteps]
+    for pdl in (False, True):
+        def body2(pdl=pdl):
+            for s, d in enumerate(lsteps):
+                if d["kind"] == "dense":
+                    snr.boundary_fused(h1, d["x"], d["post_w"], d["pre_w"], c1.n + s, c1.eps,
+                                       y=ys[s], opts=pdl_opts[pdl], stream=stream)
+                else:
+                    snr.moe_combine_boundary(h1, d["expert_out"], d["topk_w"], d["post_w"],
+                                             d["pre_w"], c1.n + s, c1.eps, y=ys[s],
+                                             opts=pdl_opts[pdl], stream=stream)
+        out[f"layer_chain104_T64_us{'_pdl' if pdl else ''}"] = timed_graph(body2, "layers", replays)
+    # the dense chain launched one call at a time, no graph
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         a.record(stream)

@@ -176,3 +176,25 @@ def moe_inputs(cfg: Config, row_start: int = 0, rows: int | None = None, pin: bo
     post_w = to_bf16(normal(cfg.seed, STREAMS["post_w"], D, 0, 0.1, 1.0))
     pre_w = to_bf16(normal(cfg.seed, STREAMS["pre_w"], D, 0, 0.1, 1.0))
     return dict(h=h, expert_out=e_out, topk_w=w, post_w=post_w, pre_w=pre_w)
+
+
+def layer_chain_inputs(chain: Config, moe: Config) -> tuple:
+    """The decode chain as a decoder runs it: boundary s (0-based, n = chain.n + s)
+    follows an attention sublayer when s is even (dense: x [T, D]) and an MoE
+    sublayer when s is odd (expert rows [T, K, D] and routing weights [T, K]:
+    tokens s*T .. s*T + T - 1 of the MoE workload's generator). Norm weights and
+    the initial stream come from dense_inputs(chain, step=s). Returns (h0, steps)."""
+    import torch
+    T = chain.T
+    h0 = dense_inputs(chain)["h"]
+    steps = []
+    for s in range(chain.steps):
+        d = dense_inputs(chain, step=s)
+        if s % 2 == 0:
+            steps.append(dict(kind="dense", x=d["x"], post_w=d["post_w"], pre_w=d["pre_w"]))
+        else:
+            r0 = s * T
+            w = topk_weights(moe.seed, STREAMS["topk"], T, moe.K, moe.route_scale, r0)
+            steps.append(dict(kind="moe", expert_out=expert_rows(moe, r0, T),
+                              topk_w=torch.from_numpy(w), post_w=d["post_w"], pre_w=d["pre_w"]))
+    return h0, steps

@@ -767,3 +767,59 @@ def test_host_memory_pageable_is_read_or_refused():
         print("pageable host memory refused (no pageable access on this device)")
         return
     check((bits(h), bits(y)), want, "pageable host memory")
+
+
+@pytest.mark.parametrize("pdl", [False, True])
+@pytest.mark.parametrize("graph", [False, True])
+def test_decoder_layer_chain_alternating_dense_and_moe_matches_the_oracle(pdl, graph):
+    """104 boundaries as the decoder runs them at T = 64: attention (dense) and MoE
+    boundaries in turn, n = 2..105, back to back on one stream (optionally one CUDA
+    graph, optionally programmatic dependent launches); every step exact."""
+    cfg = CONFIGS[1]
+    h0, steps = synth.layer_chain_inputs(cfg, CONFIGS[3])
+    dev_steps = [{k: (v.to(DEV) if k != "kind" else v) for k, v in s.items()} for s in steps]
+    h = h0.to(DEV)
+    ys = [torch.empty_like(h) for _ in steps]
+    opts = dict(flags=snr._lib.BEAM_OPT_PDL) if pdl else None
+    stream = torch.cuda.Stream()
+
+    def run_chain():
+        for s, d in enumerate(dev_steps):
+            if d["kind"] == "dense":
+                snr.boundary_fused(h, d["x"], d["post_w"], d["pre_w"], cfg.n + s, cfg.eps, y=ys[s],
+                                   opts=opts, stream=stream)
+            else:
+                snr.moe_combine_boundary(h, d["expert_out"], d["topk_w"], d["post_w"], d["pre_w"],
+                                         cfg.n + s, cfg.eps, y=ys[s], opts=opts, stream=stream)
+
+    with torch.cuda.stream(stream):
+        run_chain()  # sets up the launch shapes before any capture
+    torch.cuda.synchronize()
+    h.copy_(h0.to(DEV))
+    torch.cuda.synchronize()
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run_chain()
+        h.copy_(h0.to(DEV))
+        for y in ys:
+            y.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+    else:
+        with torch.cuda.stream(stream):
+            run_chain()
+    torch.cuda.synchronize()
+    snr.sync_status()
+
+    h_ref = oracle.as_u16(h0).copy()
+    for s, inp in enumerate(steps):
+        if inp["kind"] == "dense":
+            h_ref, y_ref = oracle.boundary(h_ref, inp["x"], inp["post_w"], inp["pre_w"], cfg.n + s,
+                                           cfg.eps, threads=THREADS)
+        else:
+            h_ref, y_ref = oracle.moe_boundary(h_ref, inp["expert_out"], inp["topk_w"],
+                                               inp["post_w"], inp["pre_w"], cfg.n + s, cfg.eps,
+                                               threads=THREADS)
+        assert_parity(bits(ys[s]), y_ref, f"layer chain step {s} ({inp['kind']}) y")
+    check((bits(h), bits(ys[-1])), (h_ref, y_ref), f"layer chain graph={graph} pdl={pdl}")
