@@ -40,7 +40,10 @@
  *   BF16 values are passed as their 16-bit patterns (uint16_t).
  *   h, x, y_out:  [T, D]       expert_out: [T, 8, D]      topk_w: [T, 8] FP32
  *   post_w, pre_w: [D]
- * All pointers are DEVICE pointers on the current device (or managed memory).
+ * All pointers are DEVICE pointers on the current device (or managed memory),
+ * except in the *_host calls, which also take page-locked host memory. The
+ * device calls check no pointer's memory type (that would cost a driver call
+ * per launch): pass host memory only to the *_host calls.
  * Every pointer must be 16-byte aligned; D must be a multiple of 8 with
  * 8 <= D <= BEAM_MAX_D.
  *
