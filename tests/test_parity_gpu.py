@@ -823,3 +823,58 @@ def test_decoder_layer_chain_alternating_dense_and_moe_matches_the_oracle(pdl, g
                                                threads=THREADS)
         assert_parity(bits(ys[s]), y_ref, f"layer chain step {s} ({inp['kind']}) y")
     check((bits(h), bits(ys[-1])), (h_ref, y_ref), f"layer chain graph={graph} pdl={pdl}")
+
+
+# --------------------------------------------------------------- seeded random shapes
+
+def _fuzz_cases(seed: int, count: int):
+    rng = np.random.default_rng(seed)
+    for _ in range(count):
+        T = int(rng.integers(1, 300))
+        D = 8 * int(rng.integers(1, 1025))            # 8 .. 8192, any multiple of 8
+        n = int(rng.integers(1, 200))
+        eps = float(rng.choice([0.0, 1e-6, 1e-5, 1e-3]))
+        scale = float(10.0 ** rng.uniform(-3, 3))
+        yield rng, T, D, n, eps, scale
+
+
+def test_random_shapes_dense_and_moe_match_the_oracle():
+    for i, (rng, T, D, n, eps, scale) in enumerate(_fuzz_cases(101, 12)):
+        inp = dict(h=bf16(rng.standard_normal((T, D))),
+                   x=bf16(rng.standard_normal((T, D)) * scale),
+                   post_w=bf16(1 + 0.3 * rng.standard_normal(D)),
+                   pre_w=bf16(1 + 0.3 * rng.standard_normal(D)))
+        if eps == 0.0:
+            inp["x"][0] = bf16(np.ones(D))  # eps = 0 only on rows that are not all zero
+        check(gpu_dense(inp, n, eps), oracle_dense(inp, n, eps), f"fuzz {i} dense T={T} D={D} n={n}")
+        m = dict(h=inp["h"], expert_out=bf16(rng.standard_normal((T, 8, D)) * scale),
+                 topk_w=torch.from_numpy(rng.uniform(0, 0.5, (T, 8)).astype(np.float32)),
+                 post_w=inp["post_w"], pre_w=inp["pre_w"])
+        check(gpu_moe(m, n, max(eps, 1e-6)), oracle_moe(m, n, max(eps, 1e-6)),
+              f"fuzz {i} moe T={T} D={D} n={n}")
+
+
+def test_random_shapes_nvfp4_match_the_oracle():
+    for i, (rng, T, D, n, eps, scale) in enumerate(_fuzz_cases(202, 10)):
+        D = 16 * max(1, D // 16)
+        gs = float(10.0 ** rng.uniform(-2, 4))
+        inp = random_dense(T, D, seed=1000 + i, scale=scale)
+        want = oracle.boundary_nvfp4(inp["h"], inp["x"], inp["post_w"], inp["pre_w"], n, 1e-6, gs)
+        check_nvfp4(gpu_dense_nvfp4(inp, n, 1e-6, gs), want, f"fuzz {i} nvfp4 T={T} D={D} gs={gs:.3g}")
+
+
+def test_random_head_counts_qk_norm_match_the_oracle():
+    rng = np.random.default_rng(303)
+    for i in range(8):
+        T, nq, nk = int(rng.integers(1, 100)), int(rng.integers(0, 64)), int(rng.integers(0, 16))
+        if nq + nk == 0:
+            nk = 1
+        q, k, qw, kw, pos, table = _qk_case(T, nq, nk, 400 + i, 3000)
+        for mode in ("rope", "ssmax"):
+            dq, dk = q.to(DEV), k.to(DEV)
+            snr.qk_norm(dq, dk, qw.to(DEV), kw.to(DEV), pos.to(DEV), 1e-6, mode,
+                        rope_table=table.to(DEV) if mode == "rope" else None)
+            snr.sync_status()
+            wq, wk = oracle.qk_norm(q, k, qw, kw, pos, table if mode == "rope" else None, 1e-6, mode)
+            assert_parity(bits(dq), wq, f"fuzz {i} qk {mode} q T={T} nq={nq}")
+            assert_parity(bits(dk), wk, f"fuzz {i} qk {mode} k T={T} nk={nk}")
