@@ -180,12 +180,16 @@ def make_inputs(device, pin: bool):
     return host, dev
 
 
-def run_step(snr, d, stream):
+def run_step(snr, d, stream, pdl: bool = False):
+    """One step: the dense then the MoE boundary. With pdl, each kernel is a
+    programmatic dependent launch: it stages its norm weights while the previous
+    kernel on the stream finishes (their weight buffers are disjoint)."""
     dn, mo = d["dense"], d["moe"]
+    opts = dict(flags=snr._lib.BEAM_OPT_PDL) if pdl else None
     snr.boundary_fused(dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, y=dn["y"],
-                       stream=stream)
+                       stream=stream, opts=opts)
     snr.moe_combine_boundary(mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"], mo["pre_w"],
-                             MOE_N, EPS, y=mo["y"], stream=stream)
+                             MOE_N, EPS, y=mo["y"], stream=stream, opts=opts)
 
 
 def decode_latency(snr, device, replays: int = 20) -> dict:
@@ -410,13 +414,12 @@ def bench_ours(args, rank, world, local_rank):
     stream = torch.cuda.Stream(device)
     host, dev = make_inputs(device, pin=True)
 
+    pdl = not args.no_pdl
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            run_step(snr, dev, stream)
+            run_step(snr, dev, stream, pdl)
     snr.sync_status(stream)
 
-    # per-kernel durations: events around each launch on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     try:
         props = torch.cuda.get_device_properties(device)
         uuid = str(getattr(props, "uuid", "") or "")
@@ -433,19 +436,36 @@ def bench_ours(args, rank, world, local_rank):
     t0 = time.time()
     with torch.cuda.stream(stream):
         start.record(stream)
-        dn, mo = dev["dense"], dev["moe"]
         for i in range(args.steps):
-            ev[i][0].record(stream)
-            snr.boundary_fused(dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS,
-                               y=dn["y"], stream=stream)
-            ev[i][1].record(stream)
-            snr.moe_combine_boundary(mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"],
-                                     mo["pre_w"], MOE_N, EPS, y=mo["y"], stream=stream)
-            ev[i][2].record(stream)
+            run_step(snr, dev, stream, pdl)
         end.record(stream)
     torch.cuda.synchronize(device)
     t1 = time.time()
     barrier(device)
+    snr.sync_status(stream)
+
+    # per-kernel durations, for the roofline: each kernel alone, back to back on
+    # the launching stream (plain launches), CUDA events around the whole loop
+    dn, mo = dev["dense"], dev["moe"]
+    kernel_steps = max(20, min(args.steps, 1000))
+
+    def per_launch_us(launch) -> float:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                launch()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(kernel_steps):
+                launch()
+            b.record(stream)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) * 1e3 / kernel_steps
+
+    dense_us = per_launch_us(lambda: snr.boundary_fused(
+        dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, y=dn["y"], stream=stream))
+    moe_us = per_launch_us(lambda: snr.moe_combine_boundary(
+        mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"], mo["pre_w"], MOE_N, EPS, y=mo["y"],
+        stream=stream))
     snr.sync_status(stream)
     time.sleep(0.2)
     sampler.stop()
@@ -453,8 +473,6 @@ def bench_ours(args, rank, world, local_rank):
     ms_total = start.elapsed_time(end)
     ms_total = max_over_ranks(ms_total, device)
     ms_step = ms_total / args.steps
-    dense_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    moe_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
 
     # end to end through the public API with the batch in host memory: page-locked
     # inputs and outputs that the kernels read and write over the CPU-GPU link
@@ -536,6 +554,10 @@ def bench_ours(args, rank, world, local_rank):
             "workload": WORKLOAD,
             "T": T_TOKENS, "D": D,
             "l2": "inputs larger than L2 (129 MB): no flush between steps",
+            "step": ("dense then MoE boundary per step, programmatic dependent launches (each "
+                     "kernel stages its weights while the previous one finishes)" if pdl else
+                     "dense then MoE boundary per step, plain launches"),
+            "per_kernel": f"each kernel alone, {kernel_steps} back-to-back plain launches, CUDA events",
             "dense": {"us": dense_us, "tokens_per_s": T_TOKENS / (dense_us * 1e-6),
                       "GBps": dense_gbs, "frac_of_measured_hbm": dense_gbs / peak,
                       "frac_of_nominal_8TBps": dense_gbs / NOMINAL_HBM_GBS, "bytes": db},
@@ -556,7 +578,7 @@ def bench_ours(args, rank, world, local_rank):
                         "CPU-GPU link",
                 "copy_then_compute": {"value": world * T_TOKENS / (copy_ms * 1e-3),
                                       "ms_per_step": copy_ms}},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * args.steps,  # in the timed region
         "clocks": clocks,
     }
     if not args.no_decode:
@@ -660,6 +682,8 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-size latency figures")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="plain launches in the timed step instead of programmatic dependent ones")
     ap.add_argument("--no-stress", action="store_true",
                     help="skip the T = 131072 MoE stress timing")
     ap.add_argument("--no-next-rows", action="store_true",
