@@ -257,10 +257,11 @@ typedef struct {
 /* Programmatic dependent launch (the following norm loads its weights before
  * its dependency wait: SGLang page, "Fusion optimizations"). The kernel may
  * start while the previous kernel on the stream is still running: it reads
- * post_w and pre_w, then waits for that kernel to finish before it touches h,
- * x, expert_out or topk_w, and lets the next kernel start its own prologue
- * early. Use it only when the kernels just before this call on the stream do
- * not write post_w or pre_w. */
+ * post_w and pre_w and asks L2 to prefetch its first rows (a hint that reads
+ * no data into the kernel), then waits for that kernel to finish before it
+ * reads h, x, expert_out or topk_w, and lets the next kernel start its own
+ * prologue early. Use it only when the kernels just before this call on the
+ * stream do not write post_w or pre_w. */
 #define BEAM_OPT_PDL 0x4u
 
 BEAM_API beam_status beam_boundary_fused_ex(beam_stream_t stream, uint16_t* h, const uint16_t* x,

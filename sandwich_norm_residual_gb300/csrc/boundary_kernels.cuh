@@ -399,9 +399,11 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
         }
     }
     if (FULL) stage_weights(p, ws_dyn);
-    pdl_wait();
+    // the L2 prefetch of this CTA's first rows: a hint that returns no data (L2
+    // is the coherence point), so it may run before the dependency wait
     if (tid == 0)
-        for (int k = 1; k < p.prefetch_rows; ++k) prefetch_row<MOE>(p, blockIdx.x + (long long)k * gridDim.x);
+        for (int k = 0; k < p.prefetch_rows; ++k) prefetch_row<MOE>(p, blockIdx.x + (long long)k * gridDim.x);
+    pdl_wait();
 
     for (long long row = blockIdx.x; row < p.T; row += gridDim.x) {
         const size_t base = (size_t)row * (size_t)p.D;
