@@ -197,7 +197,8 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
     programmatic dependent launch (PDL). T = 4: microseconds per boundary over
     200 captured calls. T = 64: microseconds per 104-boundary chain (n = 2..105,
     fresh x and weights per boundary), of dense boundaries only and of dense and
-    MoE boundaries in turn as a decoder's 52 layers run them."""
+    MoE boundaries in turn as a decoder's 52 layers run them; and per-head Q/K
+    norm with RoPE at T = 64, microseconds per layer over 52 captured launches."""
     import torch
     import synth
     from synth import CONFIGS
@@ -258,6 +259,24 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
                                              d["pre_w"], c1.n + s, c1.eps, y=ys[s],
                                              opts=pdl_opts[pdl], stream=stream)
         out[f"layer_chain104_T64_us{'_pdl' if pdl else ''}"] = timed_graph(body2, "layers", replays)
+    # per-head Q/K norm with RoPE at T = 64, one launch per layer (52), in place
+    import numpy as np
+    q64 = torch.from_numpy((synth.normal(1, 10, 64 * QK_HEADS * QK_DIM) * 2.0)
+                           .reshape(64, QK_HEADS, QK_DIM)).to(device).to(torch.bfloat16)
+    k64 = torch.from_numpy((synth.normal(1, 11, 64 * QK_KV_HEADS * QK_DIM) * 2.0)
+                           .reshape(64, QK_KV_HEADS, QK_DIM)).to(device).to(torch.bfloat16)
+    qw64 = torch.from_numpy(1 + 0.1 * synth.normal(1, 12, QK_DIM)).to(device).to(torch.bfloat16)
+    kw64 = torch.from_numpy(1 + 0.1 * synth.normal(1, 13, QK_DIM)).to(device).to(torch.bfloat16)
+    pos64 = torch.arange(1000, 1064, dtype=torch.int32, device=device)
+    inv = 10000.0 ** (-np.arange(0, QK_DIM, 2) / QK_DIM)
+    ang = np.arange(QK_SEQ)[:, None] * inv[None, :]
+    tab = torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], 1).astype(np.float32)).to(device)
+    for pdl in (False, True):
+        def body3(pdl=pdl):
+            for _ in range(52):
+                snr.qk_norm(q64, k64, qw64, kw64, pos64, 1e-6, "rope", rope_table=tab, stream=stream,
+                            pdl=pdl)
+        out[f"qk_norm_rope_T64_us_per_layer{'_pdl' if pdl else ''}"] = timed_graph(body3, "qk", replays) / 52
     # the dense chain launched one call at a time, no graph
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):

@@ -205,7 +205,10 @@ BEAM_API beam_status beam_qk_norm(beam_stream_t stream, uint16_t* q, uint16_t* k
                                   int n_q_heads, int n_kv_heads, int head_dim, float eps,
                                   int mode);
 
-/* beam_qk_norm with BEAM_OPT_* flags (only BEAM_OPT_FORCE_EXACT_SUM applies). */
+/* beam_qk_norm with BEAM_OPT_* flags: BEAM_OPT_FORCE_EXACT_SUM, and BEAM_OPT_PDL
+ * (a programmatic dependent launch: the kernel asks L2 for its tokens' rows,
+ * a hint that reads no data, then waits for the previous kernel on the stream
+ * before it reads q, k or pos). */
 BEAM_API beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k,
                                      const uint16_t* q_w, const uint16_t* k_w, const int32_t* pos,
                                      const float* rope_table, int64_t max_pos, int64_t T,

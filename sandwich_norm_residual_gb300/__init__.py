@@ -290,7 +290,7 @@ def moe_route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8
 
 
 def qk_norm(q, k, q_w, k_w, pos, eps: float = 1e-6, mode: str = "rope", rope_table=None,
-            stream=None, force_exact: bool = False):
+            stream=None, force_exact: bool = False, pdl: bool = False):
     """Per-head Q/K RMSNorm then RoPE (mode "rope") or SSMax (mode "ssmax"), in place.
 
     q: [T, n_q, 128] bf16; k: [T, n_kv, 128] bf16; q_w, k_w: [128] bf16; pos: [T] int32;
@@ -313,7 +313,8 @@ def qk_norm(q, k, q_w, k_w, pos, eps: float = 1e-6, mode: str = "rope", rope_tab
     st = _lib.load().beam_qk_norm_ex(_stream_ptr(stream), q.data_ptr(), k.data_ptr(), q_w.data_ptr(),
                                      k_w.data_ptr(), pos.data_ptr(), tab or None, max_pos, T,
                                      q.shape[1], k.shape[1], q.shape[2], float(eps), m,
-                                     _lib.BEAM_OPT_FORCE_EXACT_SUM if force_exact else 0)
+                                     (_lib.BEAM_OPT_FORCE_EXACT_SUM if force_exact else 0)
+                                     | (_lib.BEAM_OPT_PDL if pdl else 0))
     if st != 0:
         raise BeamError(st, "beam_qk_norm")
     return q, k

@@ -633,7 +633,7 @@ beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k, cons
         n_q_heads + n_kv_heads > 4096)
         return BEAM_ERR_SHAPE;
     if ((mode != BEAM_QK_ROPE && mode != BEAM_QK_SSMAX) || !(eps >= 0.0f) || !std::isfinite(eps) ||
-        (mode == BEAM_QK_ROPE && max_pos < 1) || (flags & ~BEAM_OPT_FORCE_EXACT_SUM))
+        (mode == BEAM_QK_ROPE && max_pos < 1) || (flags & ~(BEAM_OPT_FORCE_EXACT_SUM | BEAM_OPT_PDL)))
         return BEAM_ERR_ARG;
     if (T == 0 || n_q_heads + n_kv_heads == 0) return BEAM_OK;
     if ((n_q_heads && !q) || (n_kv_heads && !k) || !q_w || !k_w || !pos || (mode == BEAM_QK_ROPE && !rope_table))
@@ -666,8 +666,36 @@ beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k, cons
     p.errk = error_factor_terms(8.0, 2 + 2);  // 8 terms per FP32 lane, 2 merges in the lane + 2 shuffle levels
     p.mode = mode;
     p.flags = (flags & BEAM_OPT_FORCE_EXACT_SUM) ? beam::kFlagForceExact : 0u;
-    const int64_t blocks = (T + 7) / 8;  // 8 warps, one token each
+    // one warp per token when there are enough tokens to fill the GPU (about 24
+    // warps per SM); with fewer, up to one warp per 8-head batch of a token
+    const int nbat = (n_q_heads + n_kv_heads + beam::kQKBatch - 1) / beam::kQKBatch;
+    const int64_t target = (int64_t)info->sms * 24;
+    int wpt = 1;
+    if (T < target) {
+        const int64_t want = (target + T - 1) / T;
+        wpt = want < nbat ? (int)want : nbat;
+    }
+    p.batches_per_warp = (nbat + wpt - 1) / wpt;
+    p.warps_per_token = (nbat + p.batches_per_warp - 1) / p.batches_per_warp;
+    const int64_t blocks = (T * p.warps_per_token + 7) / 8;  // 8 warps per block
     if (blocks > 0x7FFFFFFF) return BEAM_ERR_SHAPE;
+    if (flags & BEAM_OPT_PDL) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(256);
+        cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        void* args[] = {&p};
+        if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(beam::qk_norm_kernel), args) != cudaSuccess) {
+            cudaGetLastError();
+            return BEAM_ERR_CUDA;
+        }
+        return BEAM_OK;
+    }
     beam::qk_norm_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
     if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
     return BEAM_OK;

@@ -76,13 +76,6 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
-// Programmatic dependent launch. A kernel launched with programmatic stream
-// serialisation may start while the previous kernel on the stream still runs;
-// pdl_wait() returns once that kernel has completed and its writes are
-// visible (at once when the launch had no such dependency). pdl_trigger()
-// lets the next kernel on the stream start its own prologue early.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 
 // One thread asks L2 for the inputs of row r (branch rows and h)

@@ -44,6 +44,8 @@ struct QKParams {
     float errk;
     int mode;             // 0 RoPE, 1 SSMax
     unsigned flags;       // kFlagForceExact
+    int warps_per_token;  // warps sharing a token's heads (few tokens: more warps per token)
+    int batches_per_warp; // 8-head batches each of them takes
 };
 
 // Largest SSMax position: u = (2049 + pos) / 2048 is then exact in FP32.
@@ -126,22 +128,35 @@ __device__ __noinline__ float exact_group_sum_squares(uint4 a, uint4 b, uint4 c,
 // than two batches in flight at 2 blocks per SM.
 __global__ void __launch_bounds__(256, 3) qk_norm_kernel(const QKParams p) {
     const int lane = threadIdx.x & 31, grp = lane >> 2, li = lane & 3;
-    const long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (t >= p.T) return;  // whole warps leave together
+    // warp gw takes heads [hbeg, hend) of token gw / warps_per_token
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const bool split = p.warps_per_token > 1;  // launch-uniform: no 64-bit division otherwise
+    const long long t = split ? gw / p.warps_per_token : gw;
+    const int nh = p.nq + p.nk;
+    const int hbeg = split ? (int)(gw % p.warps_per_token) * p.batches_per_warp * kQKBatch : 0;
+    const int hend = min(nh, hbeg + p.batches_per_warp * kQKBatch);
+    if (t >= p.T || hbeg >= nh) return;  // whole warps leave together
     const unsigned full = 0xFFFFFFFFu;
     const bool force_exact = (p.flags & kFlagForceExact) != 0;
+
+    // with a programmatic launch this part overlaps the previous kernel on the
+    // stream: ask L2 for this warp's q and k rows (a hint that returns no data),
+    // so that DRAM streams all of them while the batches below are loaded and
+    // processed; then wait for that kernel before reading anything
+    pdl_trigger();
+    if (lane == 0) {
+        const int qe = min(hend, p.nq), kb = max(hbeg, p.nq) - p.nq, ke = hend - p.nq;
+        if (qe > hbeg)
+            prefetch_l2(p.q + ((size_t)t * p.nq + hbeg) * kQKHeadDim, (uint32_t)(qe - hbeg) * kQKHeadDim * 2u);
+        if (ke > kb)
+            prefetch_l2(p.k + ((size_t)t * p.nk + kb) * kQKHeadDim, (uint32_t)(ke - kb) * kQKHeadDim * 2u);
+    }
+    pdl_wait();
 
     const long long pos = p.pos[t];
     if (pos < 0 || (p.mode == 0 && pos >= p.max_pos) || (p.mode != 0 && pos > kSSMaxMaxPos)) {
         if (lane == 0) atomicOr(&g_status_word, 2u);  // reported as a bad argument
         return;
-    }
-    const int nh = p.nq + p.nk;
-    // ask L2 for the token's whole q and k rows now, so that DRAM streams all
-    // its heads while the batches below are loaded and processed
-    if (lane == 0) {
-        if (p.nq) prefetch_l2(p.q + (size_t)t * p.nq * kQKHeadDim, (uint32_t)p.nq * kQKHeadDim * 2u);
-        if (p.nk) prefetch_l2(p.k + (size_t)t * p.nk * kQKHeadDim, (uint32_t)p.nk * kQKHeadDim * 2u);
     }
     auto row_of = [&](int hh) -> uint16_t* {
         return hh < p.nq ? p.q + ((size_t)t * p.nq + hh) * kQKHeadDim
@@ -160,7 +175,7 @@ __global__ void __launch_bounds__(256, 3) qk_norm_kernel(const QKParams p) {
         }
     };
     uint4 v[4];
-    load(v, 0);
+    load(v, hbeg);
 
     float2 cv[8], sv[8];
     if (p.mode == 0) {
@@ -248,8 +263,8 @@ __global__ void __launch_bounds__(256, 3) qk_norm_kernel(const QKParams p) {
         }
     };
 
-    for (int h0 = 0; h0 < nh; h0 += kQKBatch) {
-        if (h0) load(v, h0);
+    for (int h0 = hbeg; h0 < hend; h0 += kQKBatch) {
+        if (h0 != hbeg) load(v, h0);
         process(v, h0);
     }
 }

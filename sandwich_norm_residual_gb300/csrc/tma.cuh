@@ -15,6 +15,14 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialisation may start while the previous kernel on the stream still runs;
+// pdl_wait() returns once that kernel has completed and its writes are
+// visible (at once when the launch had no such dependency). pdl_trigger()
+// lets the next kernel on the stream start its own prologue early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ unsigned int g_status_word;  // bit 0: a bounded wait gave up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

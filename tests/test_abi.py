@@ -269,3 +269,15 @@ def test_host_memory_calls_check_arguments_before_cuda(lib):
     assert moe(h=E + 4096) == _lib.BEAM_ERR_ALIAS
     # valid arguments reach CUDA: without a GPU that is a CUDA or device error
     assert dense() in (_lib.BEAM_ERR_CUDA, _lib.BEAM_ERR_DEVICE)
+
+
+def test_qk_norm_flags(lib):
+    Q, K, QW, KW, P, TB = (A + (i << 32) for i in range(6))
+
+    def qk(flags):
+        return lib.beam_qk_norm_ex(None, Q, K, QW, KW, P, TB, 100, 4, 48, 8, 128, 1e-6, 0, flags)
+
+    assert qk(0x8) == _lib.BEAM_ERR_ARG                          # not a Q/K flag
+    assert qk(_lib.BEAM_OPT_TEST_WAIT_TIMEOUT) == _lib.BEAM_ERR_ARG
+    for ok in (_lib.BEAM_OPT_PDL, _lib.BEAM_OPT_FORCE_EXACT_SUM | _lib.BEAM_OPT_PDL):
+        assert qk(ok) in (_lib.BEAM_ERR_CUDA, _lib.BEAM_ERR_DEVICE)   # reaches CUDA

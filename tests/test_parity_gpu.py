@@ -878,3 +878,35 @@ def test_random_head_counts_qk_norm_match_the_oracle():
             wq, wk = oracle.qk_norm(q, k, qw, kw, pos, table if mode == "rope" else None, 1e-6, mode)
             assert_parity(bits(dq), wq, f"fuzz {i} qk {mode} q T={T} nq={nq}")
             assert_parity(bits(dk), wk, f"fuzz {i} qk {mode} k T={T} nk={nk}")
+
+
+@pytest.mark.parametrize("mode", ["rope", "ssmax"])
+def test_qk_norm_chain_with_pdl_in_a_cuda_graph(mode):
+    """Eight Q/K norms (one per layer) back to back as programmatic dependent
+    launches captured in one CUDA graph; each layer's q and k exact."""
+    layers = [_qk_case(64, 48, 8, 700 + i, 4096) for i in range(8)]
+    dev_layers = [tuple(t.to(DEV) for t in case) for case in layers]
+    stream = torch.cuda.Stream()
+
+    def run():
+        for q, k, qw, kw, pos, table in dev_layers:
+            snr.qk_norm(q, k, qw, kw, pos, 1e-6, mode, rope_table=table if mode == "rope" else None,
+                        stream=stream, pdl=True)
+
+    with torch.cuda.stream(stream):
+        run()
+    torch.cuda.synchronize()
+    for (q, k, *_), (dq, dk, *_) in zip(layers, dev_layers):
+        dq.copy_(q.to(DEV))
+        dk.copy_(k.to(DEV))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    g.replay()
+    torch.cuda.synchronize()
+    snr.sync_status()
+    for i, ((q, k, qw, kw, pos, table), (dq, dk, *_)) in enumerate(zip(layers, dev_layers)):
+        wq, wk = oracle.qk_norm(q, k, qw, kw, pos, table if mode == "rope" else None, 1e-6, mode)
+        assert_parity(bits(dq), wq, f"qk pdl layer {i} q")
+        assert_parity(bits(dk), wk, f"qk pdl layer {i} k")
