@@ -277,6 +277,16 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
                 snr.qk_norm(q64, k64, qw64, kw64, pos64, 1e-6, "rope", rope_table=tab, stream=stream,
                             pdl=pdl)
         out[f"qk_norm_rope_T64_us_per_layer{'_pdl' if pdl else ''}"] = timed_graph(body3, "qk", replays) / 52
+    # top-8 routing at T = 64, one launch per layer (52)
+    z64 = torch.from_numpy((synth.normal(1, 8, 64 * 256) * 2.0).reshape(64, 256)).to(device)
+    b64 = torch.from_numpy(synth.normal(1, 9, 256) * 0.05).to(device)
+    i64 = torch.empty((64, 8), dtype=torch.int32, device=device)
+    w64 = torch.empty((64, 8), dtype=torch.float32, device=device)
+
+    def body4():
+        for _ in range(52):
+            snr.moe_route(z64, b64, idx=i64, w=w64, stream=stream)
+    out["route_T64_us_per_layer"] = timed_graph(body4, "route", replays) / 52
     # the dense chain launched one call at a time, no graph
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
