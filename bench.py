@@ -167,8 +167,8 @@ def measured_hbm_peak() -> tuple[float, str]:
 def make_inputs(device, pin: bool):
     import torch
     import synth
-    from synth import CONFIGS
-    dense_cfg, moe_cfg = CONFIGS[2], CONFIGS[3]
+    from synth import DENSE_PREFILL_T16384, MOE_T16384
+    dense_cfg, moe_cfg = DENSE_PREFILL_T16384, MOE_T16384
     dn = synth.dense_inputs(dense_cfg)
     mo = synth.moe_inputs(moe_cfg)
     host = {"dense": dn, "moe": mo}
@@ -201,7 +201,7 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
     norm with RoPE at T = 64, microseconds per layer over 52 captured launches."""
     import torch
     import synth
-    from synth import CONFIGS
+    from synth import DECODE_CHAIN_T64, DENSE_DECODE_T4, MOE_T16384
     out = {}
     stream = torch.cuda.Stream(device)
     pdl_opts = {False: None, True: dict(flags=snr._lib.BEAM_OPT_PDL)}
@@ -223,7 +223,7 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
         torch.cuda.synchronize(device)
         return a.elapsed_time(b) * 1e3 / reps
 
-    c0 = CONFIGS[0]
+    c0 = DENSE_DECODE_T4
     d0 = {k: v.to(device) for k, v in synth.dense_inputs(c0).items()}
     y0 = torch.empty_like(d0["h"])
     for pdl in (False, True):
@@ -233,7 +233,7 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
                                    opts=pdl_opts[pdl], stream=stream)
         out[f"T4_us_per_boundary{'_pdl' if pdl else ''}"] = timed_graph(body0, "t4", replays) / 200
 
-    c1 = CONFIGS[1]
+    c1 = DECODE_CHAIN_T64
     h1 = synth.dense_inputs(c1)["h"].to(device)
     steps = [{k: v.to(device) for k, v in synth.dense_inputs(c1, step=s).items()}
              for s in range(c1.steps)]
@@ -246,7 +246,7 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
         out[f"chain104_T64_us{'_pdl' if pdl else ''}"] = timed_graph(body1, "chain", replays)
     # the chain as a decoder runs it: attention (dense) and MoE boundaries in turn
     from synth import layer_chain_inputs
-    _, lsteps = layer_chain_inputs(c1, CONFIGS[3])
+    _, lsteps = layer_chain_inputs(c1, MOE_T16384)
     lsteps = [{k: (v.to(device) if k != "kind" else v) for k, v in st.items()} for st in lsteps]
     for pdl in (False, True):
         def body2(pdl=pdl):
@@ -405,8 +405,8 @@ def moe_stress(snr, device, peak: float, reps: int = 5) -> dict:
     Inputs are generated in chunks straight into device memory."""
     import torch
     import synth
-    from synth import CONFIGS
-    cfg = CONFIGS[4]
+    from synth import MOE_STRESS_T131072
+    cfg = MOE_STRESS_T131072
     T, D, K = cfg.T, cfg.D, cfg.K
     e = torch.empty((T, K, D), dtype=torch.bfloat16, device=device)
     for r in range(0, T, 8192):
@@ -633,9 +633,9 @@ def _finish(world):
 def oracle_step_sample(rows: int, row0: int = 0):
     """Inputs of `rows` tokens of the step's workload (both boundaries)."""
     import synth
-    from synth import CONFIGS
-    return (synth.dense_inputs(CONFIGS[2], row_start=row0, rows=rows),
-            synth.moe_inputs(CONFIGS[3], row_start=row0, rows=rows))
+    from synth import DENSE_PREFILL_T16384, MOE_T16384
+    return (synth.dense_inputs(DENSE_PREFILL_T16384, row_start=row0, rows=rows),
+            synth.moe_inputs(MOE_T16384, row_start=row0, rows=rows))
 
 
 def oracle_step(dn, mo, threads: int = 1):

@@ -21,7 +21,8 @@ import threading
 
 import numpy as np
 
-from .configs import CONFIGS, Config, STREAMS  # noqa: F401
+from .configs import (DECODE_CHAIN_T64, DENSE_DECODE_T4, DENSE_PREFILL_T16384,  # noqa: F401
+                      MOE_STRESS_T131072, MOE_T16384, STREAMS, WORKLOADS, Config)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "synth.c")

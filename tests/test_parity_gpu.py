@@ -19,7 +19,8 @@ import sandwich_norm_residual_gb300 as snr
 import synth
 from parity import assert_parity, bits
 from sandwich_norm_residual_gb300 import build
-from synth import CONFIGS
+from synth import (DECODE_CHAIN_T64, DENSE_DECODE_T4, DENSE_PREFILL_T16384, MOE_STRESS_T131072,
+                   MOE_T16384)
 
 pytestmark = pytest.mark.gpu
 THREADS = max(1, min(32, os.cpu_count() or 1))
@@ -83,14 +84,14 @@ def random_dense(T, D, seed, scale=1.0):
 
 # --------------------------------------------------------------- the five workloads
 
-def test_config0_dense_decode():
-    cfg = CONFIGS[0]
+def test_dense_decode_T4():
+    cfg = DENSE_DECODE_T4
     inp = synth.dense_inputs(cfg)
     check(gpu_dense(inp, cfg.n, cfg.eps), oracle_dense(inp, cfg.n, cfg.eps), cfg.name)
 
 
-def test_config1_decode_chain_every_step_and_unit_variance():
-    cfg = CONFIGS[1]
+def test_decode_chain_T64_every_step_and_unit_variance():
+    cfg = DECODE_CHAIN_T64
     h0 = synth.dense_inputs(cfg)["h"]
     h_gpu = h0.to(DEV)
     h_ref = oracle.as_u16(h0).copy()
@@ -116,23 +117,23 @@ def test_config1_decode_chain_every_step_and_unit_variance():
     assert abs(got - pred) < 5 * sigma, (got, pred)
 
 
-def test_config2_dense_prefill_full():
-    cfg = CONFIGS[2]
+def test_dense_prefill_T16384_full():
+    cfg = DENSE_PREFILL_T16384
     inp = synth.dense_inputs(cfg)
     check(gpu_dense(inp, cfg.n, cfg.eps), oracle_dense(inp, cfg.n, cfg.eps), cfg.name)
 
 
-def test_config3_moe_full():
-    cfg = CONFIGS[3]
+def test_moe_T16384_full():
+    cfg = MOE_T16384
     inp = synth.moe_inputs(cfg)
     check(gpu_moe(inp, cfg.n, cfg.eps), oracle_moe(inp, cfg.n, cfg.eps), cfg.name)
 
 
 @pytest.mark.slow
-def test_config4_moe_stress_full_size_sampled_rows():
+def test_moe_stress_T131072_sampled_rows():
     """T = 131072 on the GPU in one launch; the oracle checks 1024 sampled rows,
     half of them tokens with a x100 outlier expert row."""
-    cfg = CONFIGS[4]
+    cfg = MOE_STRESS_T131072
     T, D, K = cfg.T, cfg.D, cfg.K
     e = torch.empty((T, K, D), dtype=torch.bfloat16, device=DEV)
     chunk = 2048
@@ -253,7 +254,7 @@ def test_launch_shape_does_not_change_a_bit():
 
 
 def test_moe_launch_shape_does_not_change_a_bit():
-    cfg = CONFIGS[3]
+    cfg = MOE_T16384
     m = synth.moe_inputs(cfg, rows=96)
     ref = gpu_moe(m, cfg.n, cfg.eps)
     check(ref, oracle_moe(m, cfg.n, cfg.eps), "moe launch-shape reference")
@@ -296,7 +297,7 @@ def test_forced_exact_path_is_bit_identical_and_counted():
     exact = gpu_dense(inp, 4, 1e-6, opts=dict(flags=snr._lib.BEAM_OPT_FORCE_EXACT_SUM))
     assert snr.exact_sum_count() == 2 * T
     assert np.array_equal(fast[0], exact[0]) and np.array_equal(fast[1], exact[1])
-    cfg = CONFIGS[3]
+    cfg = MOE_T16384
     m = synth.moe_inputs(cfg, rows=64)
     a = gpu_moe(m, cfg.n, cfg.eps)
     b = gpu_moe(m, cfg.n, cfg.eps, opts=dict(flags=snr._lib.BEAM_OPT_FORCE_EXACT_SUM))
@@ -305,7 +306,7 @@ def test_forced_exact_path_is_bit_identical_and_counted():
 
 
 def test_certification_is_rare_on_the_prefill_workload():
-    cfg = CONFIGS[2]
+    cfg = DENSE_PREFILL_T16384
     inp = synth.dense_inputs(cfg)
     snr.exact_sum_count(reset=True)
     gpu_dense(inp, cfg.n, cfg.eps)
@@ -374,7 +375,7 @@ def test_decode_chain_with_cuda_graph_and_pdl_matches_the_oracle(pdl, graph):
     """All 104 boundaries of the T = 64 decode chain back to back on one stream
     (optionally captured in one CUDA graph, optionally with programmatic
     dependent launches); every step's y and the final stream are exact."""
-    cfg = CONFIGS[1]
+    cfg = DECODE_CHAIN_T64
     h0, steps = _chain_inputs(cfg)
     dev_steps = [to_dev(s) for s in steps]
     h = h0.to(DEV)
@@ -416,11 +417,11 @@ def test_decode_chain_with_cuda_graph_and_pdl_matches_the_oracle(pdl, graph):
 
 
 def test_pdl_on_the_prefill_and_moe_workloads():
-    cfg = CONFIGS[2]
+    cfg = DENSE_PREFILL_T16384
     inp = synth.dense_inputs(cfg, rows=2048)
     opts = dict(flags=snr._lib.BEAM_OPT_PDL)
     check(gpu_dense(inp, cfg.n, cfg.eps, opts=opts), oracle_dense(inp, cfg.n, cfg.eps), "dense pdl")
-    m = synth.moe_inputs(CONFIGS[3], rows=512)
+    m = synth.moe_inputs(MOE_T16384, rows=512)
     check(gpu_moe(m, 20, 1e-6, opts=opts), oracle_moe(m, 20, 1e-6), "moe pdl")
     check(gpu_dense(inp, cfg.n, cfg.eps, opts=dict(flags=snr._lib.BEAM_OPT_PDL, stages=2)),
           oracle_dense(inp, cfg.n, cfg.eps), "dense ring pdl")
@@ -467,7 +468,7 @@ def test_routing_matches_the_oracle(ng, tg, k, scale):
 def test_routing_then_the_scaled_combine_boundary():
     """route (weights without the scale) -> boundary with the scale applied in the combine;
     and scale 1 reproduces the plain combine bit for bit."""
-    cfg = CONFIGS[3]
+    cfg = MOE_T16384
     T = 512
     z, b = _router_inputs(T, 5)
     _, w = snr.moe_route(torch.from_numpy(z).to(DEV), torch.from_numpy(b).to(DEV), route_scale=1.0)
@@ -598,7 +599,7 @@ GLOBAL_SCALES = (336.0, 1.0, 1e-3, 1e5)
 
 
 def test_nvfp4_dense_prefill_full():
-    cfg = CONFIGS[2]
+    cfg = DENSE_PREFILL_T16384
     inp = synth.dense_inputs(cfg)
     want = oracle.boundary_nvfp4(inp["h"], inp["x"], inp["post_w"], inp["pre_w"], cfg.n, cfg.eps,
                                  336.0, threads=THREADS)
@@ -606,7 +607,7 @@ def test_nvfp4_dense_prefill_full():
 
 
 def test_nvfp4_moe_full():
-    cfg = CONFIGS[3]
+    cfg = MOE_T16384
     inp = synth.moe_inputs(cfg)
     want = oracle.moe_boundary_nvfp4(inp["h"], inp["expert_out"], inp["topk_w"], inp["post_w"],
                                      inp["pre_w"], cfg.n, cfg.eps, 336.0, threads=THREADS)
@@ -657,7 +658,7 @@ def test_nvfp4_launch_shapes_forced_exact_and_pdl():
         for flags in (0, force, pdl):
             got = gpu_dense_nvfp4(inp, 9, 1e-6, 336.0, opts=dict(vec_per_thread=v, flags=flags))
             check_nvfp4(got, want, f"dense nvfp4 vpt={v} flags={flags}")
-    cfg = CONFIGS[3]
+    cfg = MOE_T16384
     m = synth.moe_inputs(cfg, rows=64)
     want = oracle.moe_boundary_nvfp4(m["h"], m["expert_out"], m["topk_w"], m["post_w"],
                                      m["pre_w"], cfg.n, cfg.eps, 336.0)
@@ -673,7 +674,7 @@ def test_nvfp4_launch_shapes_forced_exact_and_pdl():
 def test_nvfp4_agrees_with_quantising_the_bf16_output():
     """The quantised call equals the BF16 call followed by the oracle's NVFP4
     quantiser on its y, row by row."""
-    cfg = CONFIGS[3]
+    cfg = MOE_T16384
     m = synth.moe_inputs(cfg, rows=128)
     h_bf, y_bf = gpu_moe(m, cfg.n, cfg.eps)
     h_q, q, sf = gpu_moe_nvfp4(m, cfg.n, cfg.eps, 336.0)
@@ -710,7 +711,7 @@ def pinned(inp: dict) -> dict:
 def test_host_memory_dense_and_moe_full_match_the_oracle():
     """Every operand page-locked in host memory: the kernels read and write it over
     the CPU-GPU link; results equal the oracle and the device path bit for bit."""
-    cfg = CONFIGS[2]
+    cfg = DENSE_PREFILL_T16384
     inp = synth.dense_inputs(cfg)
     hp = pinned(inp)
     y = snr.boundary_fused_host(hp["h"], hp["x"], hp["post_w"], hp["pre_w"], cfg.n, cfg.eps)
@@ -718,7 +719,7 @@ def test_host_memory_dense_and_moe_full_match_the_oracle():
     assert y.device.type == "cpu" and y.is_pinned()
     want = oracle_dense(inp, cfg.n, cfg.eps)
     check((bits(hp["h"]), bits(y)), want, f"{cfg.name} host memory")
-    cfg = CONFIGS[3]
+    cfg = MOE_T16384
     m = synth.moe_inputs(cfg)
     mp = pinned(m)
     y = snr.moe_combine_boundary_host(mp["h"], mp["expert_out"], mp["topk_w"], mp["post_w"],
@@ -739,7 +740,7 @@ def test_host_memory_mixed_with_device_operands_and_a_side_stream():
         snr.boundary_fused_host(hp["h"], hp["x"], pw, qw, 5, 1e-6, y=y_dev, stream=s)
     snr.sync_status(s)
     check((bits(hp["h"]), bits(y_dev)), want, "host h and x, device weights and y")
-    cfg = CONFIGS[3]
+    cfg = MOE_T16384
     m = synth.moe_inputs(cfg, rows=200)
     wantm = oracle_moe(m, cfg.n, cfg.eps)
     e_dev = m["expert_out"].to(DEV)                                  # expert rows already on the GPU
@@ -775,8 +776,8 @@ def test_decoder_layer_chain_alternating_dense_and_moe_matches_the_oracle(pdl, g
     """104 boundaries as the decoder runs them at T = 64: attention (dense) and MoE
     boundaries in turn, n = 2..105, back to back on one stream (optionally one CUDA
     graph, optionally programmatic dependent launches); every step exact."""
-    cfg = CONFIGS[1]
-    h0, steps = synth.layer_chain_inputs(cfg, CONFIGS[3])
+    cfg = DECODE_CHAIN_T64
+    h0, steps = synth.layer_chain_inputs(cfg, MOE_T16384)
     dev_steps = [{k: (v.to(DEV) if k != "kind" else v) for k, v in s.items()} for s in steps]
     h = h0.to(DEV)
     ys = [torch.empty_like(h) for _ in steps]
