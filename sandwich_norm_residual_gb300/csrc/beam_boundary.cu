@@ -611,9 +611,13 @@ beam_status beam_moe_route(beam_stream_t stream, const float* logits, const floa
     p.topk_group = topk_group;
     p.topk = topk;
     p.scale = route_scale;
-    const int64_t blocks = (T + 7) / 8;  // 8 warps, one token each
+    const int64_t blocks = (T + beam::kRouteWarps - 1) / beam::kRouteWarps;  // one token per warp
     if (blocks > 0x7FFFFFFF) return BEAM_ERR_SHAPE;
-    beam::route_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (n_group == 8 && topk_group == 4 && topk == 8)  // the Beam / DeepSeek-V3 router
+        beam::route_kernel<8, 4, 8><<<(unsigned)blocks, 256, 0, cs>>>(p);
+    else
+        beam::route_kernel<0, 0, 0><<<(unsigned)blocks, 256, 0, cs>>>(p);
     if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
     return BEAM_OK;
 }

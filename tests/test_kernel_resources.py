@@ -62,5 +62,6 @@ def test_qk_norm_keeps_three_blocks_of_256_threads(registers):
     assert ctas_per_sm(find(registers, "qk_norm_kernel("), 256) >= 3
 
 
-def test_routing_keeps_five_blocks_of_256_threads(registers):
-    assert ctas_per_sm(find(registers, "route_kernel("), 256) >= 5
+@pytest.mark.parametrize("params", ["8, 4, 8", "0, 0, 0"])
+def test_routing_keeps_five_blocks_of_256_threads(registers, params):
+    assert ctas_per_sm(find(registers, f"route_kernel<{params}>("), 256) >= 5

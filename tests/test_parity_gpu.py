@@ -465,6 +465,34 @@ def test_routing_matches_the_oracle(ng, tg, k, scale):
                    f"route ng={ng} tg={tg} k={k}")
 
 
+@pytest.mark.parametrize("ng,tg,k", [(8, 4, 8), (4, 2, 16), (32, 4, 6)])
+def test_routing_exact_ties_go_to_the_lower_index(ng, tg, k):
+    """Logits drawn from five values with no bias: experts, and often whole groups, tie
+    exactly. Equal logits give equal scores on each side, and no two different pairs of
+    the five scores sum to nearly the same group score, so both sides see the same ties
+    and must break every one towards the lower index: identical selections on every
+    token."""
+    vals = np.array([0.3, 0.7, 1.1, 1.9, 2.6], np.float32)
+    sig = 1.0 / (1.0 + np.exp(-vals.astype(np.float64)))
+    pair_sums = np.sort([sig[i] + sig[j] for i in range(5) for j in range(i, 5)])
+    assert np.diff(pair_sums).min() > 1e-3
+    rng = np.random.default_rng(71)
+    T = 4096
+    hi = rng.integers(1, 6, (T, 8))  # group g of token t draws from the first hi values
+    z = np.empty((T, 256), np.float32)
+    for g in range(8):
+        z[:, 32 * g:32 * (g + 1)] = vals[(rng.random((T, 32)) * hi[:, g:g + 1]).astype(int)]
+    b = np.zeros(256, np.float32)
+    idx_g, w_g = snr.moe_route(torch.from_numpy(z).to(DEV), torch.from_numpy(b).to(DEV), ng, tg, k,
+                               2.5)
+    snr.sync_status()
+    idx_o, w_o = oracle.route(z, b, ng, tg, k, 2.5, threads=THREADS)
+    idx_g = idx_g.cpu().numpy()
+    assert np.array_equal(idx_g, idx_o), np.argwhere((idx_g != idx_o).any(1))[:5].ravel()
+    rel = np.abs(w_g.cpu().numpy().astype(np.float64) - w_o) / np.abs(w_o)
+    assert rel.max() <= 2.0 ** -19
+
+
 def test_routing_then_the_scaled_combine_boundary():
     """route (weights without the scale) -> boundary with the scale applied in the combine;
     and scale 1 reproduces the plain combine bit for bit."""
