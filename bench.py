@@ -38,9 +38,9 @@ WORKLOAD = (f"layer boundary pair, T={T_TOKENS} tokens per GPU, D={D}: dense bou
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "moe": {"bytes_per_launch": 1_516_889_000 + 293_180_928, "source_sha": "24998a937774a742",
+    "moe": {"bytes_per_launch": 1_516_949_000 + 292_916_224, "source_sha": "6df228e68b88af03",
             "profile": "profiles/moe_combine_boundary_T16384.md"},
-    "dense": {"bytes_per_launch": 335_718_000 + 275_040_256, "source_sha": "24998a937774a742",
+    "dense": {"bytes_per_launch": 335_719_000 + 275_428_096, "source_sha": "6df228e68b88af03",
               "profile": "profiles/dense_boundary_T16384.md"},
 }
 

@@ -75,11 +75,43 @@ __device__ __forceinline__ void pick_rounds(uint32_t (&key)[NK], uint32_t base, 
     }
 }
 
+// The same rounds over 4 keys per lane (expert base + i), sorted once: then a
+// lane's best key is its first, and the lane that wins a round shifts its
+// list by one. The sort ranks larger keys first and, among equal keys, the
+// lower index, so every round picks what pick_rounds would.
+__device__ __forceinline__ void pick_rounds_sorted4(uint32_t (&key)[4], uint32_t base, int topk, int lane,
+                                                    int (&sel_i)[kRouteMaxTopk], int& my_i) {
+    const unsigned full = 0xFFFFFFFFu;
+    uint32_t ix[4] = {0u, 1u, 2u, 3u};
+    auto order = [&](int a, int b) {  // afterwards (key[a], ix[a]) ranks before (key[b], ix[b])
+        const bool sw = key[b] > key[a] || (key[b] == key[a] && ix[b] < ix[a]);
+        const uint32_t ka = sw ? key[b] : key[a], kb = sw ? key[a] : key[b];
+        const uint32_t ia = sw ? ix[b] : ix[a], ib = sw ? ix[a] : ix[b];
+        key[a] = ka; key[b] = kb; ix[a] = ia; ix[b] = ib;
+    };
+    order(0, 1); order(2, 3); order(0, 2); order(1, 3); order(1, 2);
+    uint32_t ixp = ix[0] | (ix[1] << 2) | (ix[2] << 4) | (ix[3] << 6);  // 2 bits per list entry
+#pragma unroll
+    for (int k = 0; k < kRouteMaxTopk; ++k) {
+        if (k >= topk) break;
+        const uint32_t mine = base + (ixp & 3u);
+        const uint32_t m = __reduce_max_sync(full, key[0]);
+        const uint32_t e = __reduce_min_sync(full, (key[0] == m) ? mine : 0xFFFFFFFFu);
+        if (e == mine) {
+            key[0] = key[1]; key[1] = key[2]; key[2] = key[3]; key[3] = 0u;
+            ixp >>= 2;
+        }
+        sel_i[k] = (int)e;
+        if (lane == k) my_i = (int)e;
+    }
+}
+
 // NG, TG, K: n_group, topk_group and topk fixed at compile time (0: read from
 // the parameters). Fixed values unroll every loop and turn the group arithmetic
 // into shifts; the arithmetic on the scores is the same either way. When the
 // kept groups hold 128 experts, they are first compacted in shared memory to 4
-// per lane, which halves the work of every topk round.
+// per lane and sorted within the lane, which makes each topk round two warp
+// reductions and a shift.
 template <int NG, int TG, int K>
 __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
     constexpr bool kCompact = NG > 0 && TG > 0 && TG * (kRouteExperts / (NG > 0 ? NG : 1)) == 128;
@@ -157,7 +189,7 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
         __syncwarp();
         const float4 v = reinterpret_cast<const float4*>(ck[warp])[lane];
         uint32_t key[4] = {order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w)};
-        pick_rounds<4>(key, (uint32_t)(cb[warp][lane >> 1] + 4 * (lane & 1)), topk, lane, sel_i, my_i);
+        pick_rounds_sorted4(key, (uint32_t)(cb[warp][lane >> 1] + 4 * (lane & 1)), topk, lane, sel_i, my_i);
     } else {
         uint32_t key[8];
 #pragma unroll
