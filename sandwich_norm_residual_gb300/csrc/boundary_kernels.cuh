@@ -192,10 +192,20 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
     return f;
 }
 
-// two FP32 -> two E2M1 codes, nearest even, saturating: lo in bits 0-3, hi in 4-7
-__device__ __forceinline__ uint32_t f2_to_e2m1x2(float lo, float hi) {
+// eight FP32 -> eight E2M1 codes, nearest even, saturating: value 2i in the
+// low nibble of byte i, value 2i+1 in its high nibble (the pairs are packed
+// straight into the word)
+__device__ __forceinline__ uint32_t f8_to_e2m1x8(const float2 (&v)[4]) {
     uint32_t r;
-    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+    asm("{ .reg .b8 t0, t1, t2, t3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3}; }"
+        : "=r"(r)
+        : "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y), "f"(v[3].x),
+          "f"(v[3].y));
     return r;
 }
 
@@ -352,11 +362,10 @@ __device__ __forceinline__ void finish_row(const BoundaryParams& p, long long ro
             if (sfb != 0u) {  // code 0 is the only zero scale (the argument is >= 0)
                 const float inv = rs->inv_sf[sfb & 0x7Fu];
                 const float2 iv = make_float2(inv, inv);
+                float2 f[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 f = mul2_rn(bf2_to_f2(word(yv, q)), iv);
-                    codes |= f2_to_e2m1x2(f.x, f.y) << (8 * q);
-                }
+                for (int q = 0; q < 4; ++q) f[q] = mul2_rn(bf2_to_f2(word(yv, q)), iv);
+                codes = f8_to_e2m1x8(f);
             }
             if (valid) {
                 *reinterpret_cast<uint32_t*>(p.yq + (base + (size_t)vi * 8) / 2) = codes;
