@@ -38,9 +38,9 @@ WORKLOAD = (f"layer boundary pair, T={T_TOKENS} tokens per GPU, D={D}: dense bou
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "moe": {"bytes_per_launch": 1_516_949_000 + 292_916_224, "source_sha": "6df228e68b88af03",
+    "moe": {"bytes_per_launch": 1_516_914_000 + 292_385_536, "source_sha": "9bb3976ec3c1cf4f",
             "profile": "profiles/moe_combine_boundary_T16384.md"},
-    "dense": {"bytes_per_launch": 335_719_000 + 275_428_096, "source_sha": "6df228e68b88af03",
+    "dense": {"bytes_per_launch": 335_698_000 + 275_089_408, "source_sha": "9bb3976ec3c1cf4f",
               "profile": "profiles/dense_boundary_T16384.md"},
 }
 
