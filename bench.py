@@ -44,6 +44,12 @@ NCU_TRAFFIC = {
               "profile": "profiles/dense_boundary_T16384.md"},
 }
 
+# Routing is bound by instruction issue, not HBM: its warp-instructions per
+# launch at T = 16384 (ncu smsp__inst_executed.sum) give its issue roofline,
+# valid while the kernel source matches.
+ROUTE_ISSUE = {"warp_instructions_per_launch": 8_699_904, "source_sha": "9bb3976ec3c1cf4f",
+               "profile": "profiles/route_T16384.md"}
+
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
@@ -337,11 +343,12 @@ def _time_launches(fn, stream, reps: int, warmup: int = 3) -> float:
     return a.elapsed_time(e) * 1e3 / reps
 
 
-def next_rows(snr, device, dev, peak: float) -> dict:
+def next_rows(snr, device, dev, peak: float, sm_mhz: float | None = None) -> dict:
     """The scope table's next rows at T = 16384, each timed on its own and
     reported beside the step (none is part of it): group-limited top-8 routing,
     per-head Q/K norm with RoPE or SSMax (8 sequences of 2048 positions), and
-    the two boundaries with y written as NVFP4."""
+    the two boundaries with y written as NVFP4. Routing also reports its issue
+    roofline: 4 warp-instructions per SM per clock at `sm_mhz`."""
     import torch
     import synth
     stream = torch.cuda.Stream(device)
@@ -361,7 +368,14 @@ def next_rows(snr, device, dev, peak: float) -> dict:
     w = torch.empty((T, 8), dtype=torch.float32, device=device)
     us = _time_launches(lambda i: snr.moe_route(z[i % nbuf], b, idx=idx, w=w, stream=stream),
                         stream, 50)
-    out["route_top8_of_256"] = entry(us, route_bytes(T))
+    rt = entry(us, route_bytes(T))
+    if sm_mhz and ROUTE_ISSUE["source_sha"] == kernel_source_sha():
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        issue_peak = sms * 4 * sm_mhz * 1e6  # warp-instructions per second
+        inst = ROUTE_ISSUE["warp_instructions_per_launch"]
+        rt.update({"bound": "issue", "warp_instructions": inst, "issue_peak_per_s": issue_peak,
+                   "frac_of_issue_peak": round(inst / (us * 1e-6) / issue_peak, 4)})
+    out["route_top8_of_256"] = rt
     del z
 
     # Q/K norm: q [T, 48, 128] and k [T, 8, 128] (235 MB together, above L2)
@@ -613,7 +627,8 @@ def bench_ours(args, rank, world, local_rank):
     if not args.no_decode:
         line["config"]["decode"] = decode_latency(snr, device)
     if not args.no_next_rows:
-        line["config"]["next_rows"] = next_rows(snr, device, dev, peak)
+        line["config"]["next_rows"] = next_rows(snr, device, dev, peak,
+                                                clocks.get("sm_mhz") or clocks.get("sm_max_mhz"))
     if not args.no_stress:
         line["config"]["moe_stress_T131072"] = moe_stress(snr, device, peak)
     if not args.no_cpu_baseline:
