@@ -469,8 +469,10 @@ int oracle_qk_norm(bf16_t* q, bf16_t* k, const bf16_t* qw, const bf16_t* kw, con
  *   inv  = RN32(gs / sf)                              one division per block
  *   q_j  = sf == 0 ? +0 : E2M1(RN32(y_j * inv))
  * Both conversions are written out as a nearest search over the format's
- * finite values (ties to the even code, magnitudes above the largest value
- * saturate, the sign is kept).
+ * finite values (ties to the even code, magnitudes above the largest value,
+ * infinities included, saturate; the sign is kept). A NaN converts to E4M3's
+ * NaN code 0x7F; E2M1 has no NaN, and a NaN converts to +6 (code 0x7), as
+ * NVIDIA's saturating conversion does. The block amax skips NaN values.
  * ---------------------------------------------------------------------- */
 
 static float e4m3_value(unsigned code) { /* finite codes 0..0x7E of the magnitude */
@@ -485,6 +487,9 @@ static float e2m1_value(unsigned code) {
 
 /* nearest code (magnitude) among n_codes values, ties to the even code; saturates */
 static unsigned nearest_code(float mag, float (*value)(unsigned), unsigned n_codes) {
+    /* saturating: the largest value and anything beyond it, infinity included
+     * (a distance search would tie once the distances round alike) */
+    if (mag >= value(n_codes - 1)) return n_codes - 1;
     unsigned best = 0;
     double bd = fabs((double)mag - (double)value(0));
     for (unsigned c = 1; c < n_codes; ++c) {
@@ -495,11 +500,13 @@ static unsigned nearest_code(float mag, float (*value)(unsigned), unsigned n_cod
 }
 
 uint8_t oracle_e4m3(float v) {
+    if (isnan(v)) return 0x7F;
     unsigned s = signbit(v) ? 0x80u : 0u;
     return (uint8_t)(s | nearest_code(fabsf(v), e4m3_value, 0x7F));
 }
 
 uint8_t oracle_e2m1(float v) {
+    if (isnan(v)) return 0x7;
     unsigned s = signbit(v) ? 0x8u : 0u;
     return (uint8_t)(s | nearest_code(fabsf(v), e2m1_value, 8));
 }

@@ -89,6 +89,10 @@ MUTANTS = [
      "if (d < bd || (d == bd && c > best)) { best = c; bd = d; }"),
     ("NVFP4 quantises with the global scale inverted", "const float inv = sv != 0.0f ? gs / sv : 0.0f;",
      "const float inv = sv != 0.0f ? 1.0f / (gs * sv) : 0.0f;"),
+    ("FP8/FP4 saturation left to the distance search",
+     "    if (mag >= value(n_codes - 1)) return n_codes - 1;\n", ""),
+    ("NVFP4 block max takes NaN", "if (a > amax) amax = a;", "if (!(a <= amax)) amax = a;"),
+    ("E2M1 NaN encoded as zero", "    if (isnan(v)) return 0x7;\n", "    if (isnan(v)) return 0x0;\n"),
     ("long-double residual coefficient squared",
      "long double c1 = sqrtl((long double)(n - 1) / (long double)n);\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i",
      "long double c1 = (long double)(n - 1) / (long double)n;\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i"),

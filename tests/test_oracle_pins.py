@@ -727,6 +727,33 @@ def test_e2m1_rounding_table():
     assert oracle.e2m1(-0.1) == 0x8   # the sign is kept (-0)
 
 
+def test_e4m3_and_e2m1_saturate_all_the_way_to_infinity():
+    """Saturation holds for every magnitude beyond the largest value, infinity
+    included (a nearest-distance search would tie once the distances round alike)."""
+    for v in (448.0, 449.0, 1e6, 1e17, 1e20, 3.4e38, math.inf):
+        assert oracle.e4m3(v) == 0x7E and oracle.e4m3(-v) == 0xFE, v
+    for v in (6.0, 6.5, 1e9, 1e17, 1e20, 3.4e38, math.inf):
+        assert oracle.e2m1(v) == 0x7 and oracle.e2m1(-v) == 0xF, v
+
+
+def test_nan_codes_follow_the_reading():
+    # E4M3FN keeps NaN as 0x7F; E2M1 has no NaN, and a NaN converts to +6 (0x7),
+    # as the hardware's saturating conversion does
+    assert oracle.e4m3(math.nan) == 0x7F
+    assert oracle.e2m1(math.nan) == 0x7
+
+
+def test_nvfp4_block_amax_skips_nan_and_an_infinite_amax_saturates_the_scale():
+    y = np.zeros(32, np.float32)
+    y[:4] = [math.inf, 1.0, -2.0, math.nan]  # amax inf: scale 448; codes +6, 0, -0, +6
+    y[16:18] = [math.nan, 3.0]               # amax 3 (NaN skipped): scale 0.5; +6, 6
+    q, sf = oracle.nvfp4_row(bf16_bits(y), 1.0)
+    assert sf[0] == 0x7E and oracle.e4m3_to_f32(int(sf[1])) == 0.5
+    nib = [int(q[i // 2]) >> (4 * (i % 2)) & 0xF for i in range(32)]
+    assert nib[:4] == [0x7, 0x0, 0x8, 0x7] and nib[4:16] == [0] * 12
+    assert nib[16:18] == [0x7, 0x7] and nib[18:] == [0] * 14
+
+
 def test_nvfp4_hand_block():
     # gs = 1, amax = 3: sf = e4m3(3/6) = 0.5, q = e2m1(2 y)
     y = np.array([1, 2, 3, -1, 0.25, 0, -3, 0.5, 1.5, -2, 0.125, 0, 0, 0, 0, 0.75], np.float32)
