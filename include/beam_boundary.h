@@ -295,7 +295,9 @@ BEAM_API beam_status beam_moe_combine_boundary_ex(beam_stream_t stream, uint16_t
  * opts may be NULL; options of the shared-memory ring (stages > 0, the wait
  * timeout hook) give BEAM_ERR_ARG. y_fp4 and y_scale overlap neither each other
  * nor any other operand.
- * y must be finite for the codes to be defined.
+ * Non-finite y: the block amax skips NaN values; an infinite amax gives the
+ * saturated scale 448 (0x7E) and infinite values the codes +-6; a NaN value's
+ * code is +6 (0x7), since E2M1 has no NaN.
  */
 BEAM_API beam_status beam_boundary_fused_nvfp4(beam_stream_t stream, uint16_t* h, const uint16_t* x,
                                       const uint16_t* post_w, const uint16_t* pre_w, int n,

@@ -215,11 +215,14 @@ __device__ __forceinline__ uint32_t f8_to_e2m1x8(const float2 (&v)[4]) {
 // t + r c (Markstein's correction step for a known divisor) rounds correctly:
 // a/6 = (significand / 3) 2^k always lies at least 1/6 ulp from a rounding
 // midpoint, far beyond the correction's error. Checked for every non-negative
-// BF16 value in exact rational arithmetic.
+// finite BF16 value in exact rational arithmetic. For a = +inf, t is +inf
+// (a finite a never makes t overflow) and is returned as it is: the correction
+// would give inf - inf = NaN.
 __device__ __forceinline__ float div6_bf16(float a) {
     const float c = 0x1.555556p-3f;
     const float t = __fmul_rn(a, c);
-    return __fmaf_rn(__fmaf_rn(-t, 6.0f, a), c, t);
+    const float q = __fmaf_rn(__fmaf_rn(-t, 6.0f, a), c, t);
+    return t < INFINITY ? q : t;
 }
 
 // h is read and later overwritten by the same thread; this form also keeps

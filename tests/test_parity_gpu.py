@@ -699,6 +699,33 @@ def test_nvfp4_launch_shapes_forced_exact_and_pdl():
             check_nvfp4(got, want, f"moe nvfp4 vpt={v} flags={flags}")
 
 
+def test_nvfp4_non_finite_values_match_the_oracle():
+    """Rows whose y is all NaN (NaN or -inf in x), a row with an infinite h, and
+    pre-norm weights holding a NaN and +-inf, which put NaN and infinite values
+    in blocks of every other row: the block amax skips NaN, an infinite amax
+    saturates the scale, infinite values saturate their codes and a NaN value's
+    code is +6 (0x7)."""
+    rng = np.random.default_rng(81)
+    T, D = 6, 256
+    inp = random_dense(T, D, seed=81)
+    inp["x"][0, 7] = float("nan")
+    inp["h"][1, 9] = float("inf")
+    inp["x"][2, 3] = float("-inf")
+    inp["pre_w"][5] = float("nan")
+    inp["pre_w"][40] = float("inf")
+    inp["pre_w"][41] = float("-inf")
+    want = oracle.boundary_nvfp4(inp["h"], inp["x"], inp["post_w"], inp["pre_w"], 3, 1e-6, 336.0)
+    assert (want[2] == 0x7E).any() and (want[1] == 0x77).any()  # the cases are present
+    check_nvfp4(gpu_dense_nvfp4(inp, 3, 1e-6, 336.0), want, "dense nvfp4 non-finite")
+    m = dict(h=inp["h"], expert_out=bf16(rng.standard_normal((T, 8, D))),
+             topk_w=torch.from_numpy(rng.uniform(0, 0.4, (T, 8)).astype(np.float32)),
+             post_w=inp["post_w"], pre_w=inp["pre_w"])
+    m["expert_out"][0, 3, 11] = float("nan")
+    want = oracle.moe_boundary_nvfp4(m["h"], m["expert_out"], m["topk_w"], m["post_w"], m["pre_w"],
+                                     3, 1e-6, 336.0)
+    check_nvfp4(gpu_moe_nvfp4(m, 3, 1e-6, 336.0), want, "moe nvfp4 non-finite")
+
+
 def test_nvfp4_agrees_with_quantising_the_bf16_output():
     """The quantised call equals the BF16 call followed by the oracle's NVFP4
     quantiser on its y, row by row."""
