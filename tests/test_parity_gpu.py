@@ -17,7 +17,7 @@ import torch
 import oracle
 import sandwich_norm_residual_gb300 as snr
 import synth
-from parity import assert_parity, bits
+from parity import assert_parity, bits, compare
 from sandwich_norm_residual_gb300 import build
 from synth import (DECODE_CHAIN_T64, DENSE_DECODE_T4, DENSE_PREFILL_T16384, MOE_STRESS_T131072,
                    MOE_T16384)
@@ -547,6 +547,27 @@ def test_qk_norm_matches_the_oracle(mode, T, nq, nk):
     st_q = assert_parity(bits(dq), wq, f"qk {mode} q") if nq else None
     st_k = assert_parity(bits(dk), wk, f"qk {mode} k") if nk else None
     print(f"qk_norm {mode} T={T} nq={nq} nk={nk}: q {st_q} k {st_k}")
+
+
+@pytest.mark.parametrize("mode", ["rope", "ssmax"])
+def test_qk_norm_non_finite_and_zero_heads_match_the_oracle(mode):
+    """Beside finite heads: a NaN element (its head goes NaN), +-inf elements (the
+    head's factor is 0, so NaN at the element, and under RoPE at its rotation
+    partner, zeros elsewhere) and an all-zero head; every output identical."""
+    q, k, qw, kw, pos, table = _qk_case(9, 48, 8, 91, 512)
+    q[0, 1, 7] = float("nan")
+    q[1, 0, 70] = float("inf")
+    k[2, 1, 3] = float("-inf")
+    q[3, 2, :] = 0.0
+    k[4, 0, 64] = float("nan")
+    dq, dk = q.to(DEV), k.to(DEV)
+    snr.qk_norm(dq, dk, qw.to(DEV), kw.to(DEV), pos.to(DEV), 1e-6, mode,
+                rope_table=table.to(DEV) if mode == "rope" else None)
+    snr.sync_status()
+    wq, wk = oracle.qk_norm(q, k, qw, kw, pos, table if mode == "rope" else None, 1e-6, mode)
+    for got, want, name in ((bits(dq), wq, "q"), (bits(dk), wk, "k")):
+        st = compare(got, want)
+        assert st["frac_identical"] == 1.0, (mode, name, st)
 
 
 def test_ssmax_scale_at_every_position_below_a_million():
