@@ -167,7 +167,8 @@ BEAM_API beam_status beam_moe_combine_boundary_scaled(beam_stream_t stream, uint
  * Logits must not be NaN (the choice among NaN scores is unspecified).
  * exp is CUDA's FP32 expf, so s_e may differ from the correctly rounded
  * sigmoid by a few ulps, and an exact tie between two biased scores may then
- * break the other way.
+ * break the other way. Below a logit of about -88.7, expf(-logit) overflows
+ * and s_e is 0, where the correctly rounded value is a subnormal under 3e-39.
  */
 BEAM_API beam_status beam_moe_route(beam_stream_t stream, const float* logits, const float* bias,
                                     int64_t T, int E, int n_group, int topk_group, int topk,

@@ -465,6 +465,24 @@ def test_routing_matches_the_oracle(ng, tg, k, scale):
                    f"route ng={ng} tg={tg} k={k}")
 
 
+def test_routing_with_infinite_and_extreme_logits():
+    """Logits of +-inf, +-100 and +-50 beside ordinary ones: the sigmoid saturates
+    to exactly 1 or underflows (the kernel's is 0 below about -88.7, where the
+    correctly rounded value is a subnormal under 3e-39, far below any bias), and the
+    routing stays within the tolerance of the random-logit test."""
+    T = 2048
+    z, b = _router_inputs(T, 13)
+    rng = np.random.default_rng(13)
+    extremes = np.array([np.inf, -np.inf, 100.0, -100.0, 50.0, -50.0], np.float32)
+    pick = rng.random((T, 256)) < 0.05
+    z[pick] = extremes[rng.integers(0, extremes.size, int(pick.sum()))]
+    idx_g, w_g = snr.moe_route(torch.from_numpy(z).to(DEV), torch.from_numpy(b).to(DEV))
+    snr.sync_status()
+    idx_o, w_o = oracle.route(z, b, threads=THREADS)
+    assert np.isfinite(w_g.cpu().numpy()).all()
+    _check_routing(z, b, idx_g.cpu().numpy(), w_g.cpu().numpy(), idx_o, w_o, "route extreme logits")
+
+
 @pytest.mark.parametrize("ng,tg,k", [(8, 4, 8), (4, 2, 16), (32, 4, 6)])
 def test_routing_exact_ties_go_to_the_lower_index(ng, tg, k):
     """Logits drawn from five values with no bias: experts, and often whole groups, tie
