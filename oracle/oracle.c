@@ -512,6 +512,7 @@ uint8_t oracle_e2m1(float v) {
 }
 
 float oracle_e4m3_to_f32(uint8_t b) {
+    if ((b & 0x7Fu) == 0x7Fu) return NAN; /* E4M3FN: S.1111.111 is NaN (there is no infinity) */
     float m = e4m3_value(b & 0x7Fu);
     return (b & 0x80u) ? -m : m;
 }

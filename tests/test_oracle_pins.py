@@ -717,6 +717,14 @@ def test_e4m3_matches_torch_float8_cast_in_range():
     assert oracle.e4m3_to_f32(oracle.e4m3(-470.0)) == -448.0
 
 
+def test_e4m3_decoder_matches_torch_on_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    got = np.array([oracle.e4m3_to_f32(int(c)) for c in codes], np.float32)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.array_equal(got[~np.isnan(got)], want[~np.isnan(want)])
+
+
 def test_e2m1_rounding_table():
     # the eight magnitudes 0 0.5 1 1.5 2 3 4 6; halfway cases go to the even code
     cases = {0.25: 0.0, 0.26: 0.5, 0.75: 1.0, 1.25: 1.0, 1.3: 1.5, 1.75: 2.0, 2.5: 2.0,
@@ -741,6 +749,9 @@ def test_nan_codes_follow_the_reading():
     # as the hardware's saturating conversion does
     assert oracle.e4m3(math.nan) == 0x7F
     assert oracle.e2m1(math.nan) == 0x7
+    # E4M3FN has no infinity: S.1111.111 is NaN, and 0x7E = 448 is the largest value
+    assert math.isnan(oracle.e4m3_to_f32(0x7F)) and math.isnan(oracle.e4m3_to_f32(0xFF))
+    assert oracle.e4m3_to_f32(0x7E) == 448.0 and oracle.e4m3_to_f32(0xFE) == -448.0
 
 
 def test_nvfp4_block_amax_skips_nan_and_an_infinite_amax_saturates_the_scale():
