@@ -93,6 +93,12 @@ MUTANTS = [
      "    if (mag >= value(n_codes - 1)) return n_codes - 1;\n", ""),
     ("NVFP4 block max takes NaN", "if (a > amax) amax = a;", "if (!(a <= amax)) amax = a;"),
     ("E2M1 NaN encoded as zero", "    if (isnan(v)) return 0x7;\n", "    if (isnan(v)) return 0x0;\n"),
+    ("routing keeps one group too many", "for (int k = 0; k < topk_group; ++k) {",
+     "for (int k = 0; k <= topk_group && k < n_group; ++k) {"),
+    ("RoPE cross term with the cosine", "bc = b * c, as = a * s;", "bc = b * c, as = a * c;"),
+    ("SSMax exponent 0.2", "(double)(pos + 1) / 2048.0, 0.1);", "(double)(pos + 1) / 2048.0, 0.2);"),
+    ("E4M3 subnormals one binade low", "ldexpf((float)m / 8.0f, -6)", "ldexpf((float)m / 8.0f, -7)"),
+    ("E2M1 smallest step 0.25", "(m ? 0.5f : 0.0f)", "(m ? 0.25f : 0.0f)"),
     ("long-double residual coefficient squared",
      "long double c1 = sqrtl((long double)(n - 1) / (long double)n);\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i",
      "long double c1 = (long double)(n - 1) / (long double)n;\n    long double c2 = 1.0L / sqrtl((long double)n);\n    for (int64_t i"),
