@@ -41,15 +41,37 @@ def _stream_ptr(stream) -> int | None:
 
 
 def _check(t, name: str, dtype, ndim: int):
+    """Type, dtype, rank and layout of one operand (devices: ``_on_current_device``)."""
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
-        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
     if t.dim() != ndim or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def _shape(t, name: str, shape: tuple):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)} (got {tuple(t.shape)})")
+
+
+def _on_current_device(**tensors):
+    """Every operand on one CUDA device, the current one: the library launches on the
+    current device and takes the pointers as they are, so a tensor elsewhere would
+    reach the kernel as a foreign address. Checked after the shapes, before any launch."""
+    import torch
+    devs = {name: t.device for name, t in tensors.items()}
+    if len(set(devs.values())) != 1:
+        raise ValueError("operands must all be on one device: "
+                         + ", ".join(f"{n} on {d}" for n, d in devs.items()))
+    dev = next(iter(devs.values()))
+    if dev.type != "cuda":
+        raise ValueError(f"operands must be CUDA tensors (got {dev})")
+    cur = torch.cuda.current_device()
+    if dev.index != cur:
+        raise ValueError(f"operands are on {dev} but the current device is cuda:{cur}: "
+                         f"call under `with torch.cuda.device({dev.index}):`")
 
 
 def _opts(opts):
@@ -76,6 +98,8 @@ def boundary_fused(h, x, post_w, pre_w, n: int, eps: float = 1e-6, y=None, strea
     if y is None:
         y = torch.empty_like(h)
     _check(y, "y", torch.bfloat16, 2)
+    _shape(y, "y", (T, D))
+    _on_current_device(h=h, x=x, post_w=post_w, pre_w=pre_w, y=y)
     lib = _lib.load()
     args = (_stream_ptr(stream), h.data_ptr(), x.data_ptr(), post_w.data_ptr(), pre_w.data_ptr(),
             int(n), float(eps), T, D, y.data_ptr())
@@ -109,6 +133,8 @@ def moe_combine_boundary(h, expert_out, topk_w, post_w, pre_w, n: int, eps: floa
     if y is None:
         y = torch.empty_like(h)
     _check(y, "y", torch.bfloat16, 2)
+    _shape(y, "y", (T, D))
+    _on_current_device(h=h, expert_out=expert_out, topk_w=topk_w, post_w=post_w, pre_w=pre_w, y=y)
     lib = _lib.load()
     if route_scale is not None:
         if opts is not None:
@@ -167,6 +193,7 @@ def boundary_fused_host(h, x, post_w, pre_w, n: int, eps: float = 1e-6, y=None, 
     if y is None:
         y = _like_host(h)
     _check_any(y, "y", torch.bfloat16, 2)
+    _shape(y, "y", (T, D))
     st = _lib.load().beam_boundary_fused_host(_stream_ptr(stream), h.data_ptr(), x.data_ptr(),
                                               post_w.data_ptr(), pre_w.data_ptr(), int(n),
                                               float(eps), T, D, y.data_ptr())
@@ -192,6 +219,7 @@ def moe_combine_boundary_host(h, expert_out, topk_w, post_w, pre_w, n: int, eps:
     if y is None:
         y = _like_host(h)
     _check_any(y, "y", torch.bfloat16, 2)
+    _shape(y, "y", (T, D))
     st = _lib.load().beam_moe_combine_boundary_host(
         _stream_ptr(stream), h.data_ptr(), expert_out.data_ptr(), topk_w.data_ptr(),
         post_w.data_ptr(), pre_w.data_ptr(), int(n), float(eps), T, D, y.data_ptr())
@@ -229,6 +257,7 @@ def boundary_fused_nvfp4(h, x, post_w, pre_w, n: int, eps: float, y_global_scale
     if x.shape != h.shape or post_w.shape[0] != D or pre_w.shape[0] != D:
         raise ValueError("shape mismatch: h, x [T, D]; post_w, pre_w [D]")
     q, sf = _nvfp4_out(h, y_fp4, y_scale)
+    _on_current_device(h=h, x=x, post_w=post_w, pre_w=pre_w, y_fp4=q, y_scale=sf)
     st = _lib.load().beam_boundary_fused_nvfp4(_stream_ptr(stream), h.data_ptr(), x.data_ptr(),
                                                post_w.data_ptr(), pre_w.data_ptr(), int(n),
                                                float(eps), T, D, float(y_global_scale),
@@ -253,6 +282,8 @@ def moe_combine_boundary_nvfp4(h, expert_out, topk_w, post_w, pre_w, n: int, eps
             or post_w.shape[0] != D or pre_w.shape[0] != D):
         raise ValueError("shape mismatch: h [T, D]; expert_out [T, 8, D]; topk_w [T, 8]")
     q, sf = _nvfp4_out(h, y_fp4, y_scale)
+    _on_current_device(h=h, expert_out=expert_out, topk_w=topk_w, post_w=post_w, pre_w=pre_w,
+                       y_fp4=q, y_scale=sf)
     st = _lib.load().beam_moe_combine_boundary_nvfp4(
         _stream_ptr(stream), h.data_ptr(), expert_out.data_ptr(), topk_w.data_ptr(),
         post_w.data_ptr(), pre_w.data_ptr(), int(n), float(eps), T, D, float(y_global_scale),
@@ -281,6 +312,9 @@ def moe_route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8
         w = torch.empty((T, topk), dtype=torch.float32, device=logits.device)
     _check(idx, "idx", torch.int32, 2)
     _check(w, "w", torch.float32, 2)
+    _shape(idx, "idx", (T, topk))
+    _shape(w, "w", (T, topk))
+    _on_current_device(logits=logits, bias=bias, idx=idx, w=w)
     st = _lib.load().beam_moe_route(_stream_ptr(stream), logits.data_ptr(), bias.data_ptr(), T, E,
                                     int(n_group), int(topk_group), int(topk), float(route_scale),
                                     idx.data_ptr(), w.data_ptr())
@@ -305,11 +339,19 @@ def qk_norm(q, k, q_w, k_w, pos, eps: float = 1e-6, mode: str = "rope", rope_tab
     T = q.shape[0]
     if k.shape[0] != T or pos.shape[0] != T or q.shape[2] != k.shape[2]:
         raise ValueError("shape mismatch: q [T, nq, 128], k [T, nk, 128], pos [T]")
+    hd = q.shape[2]
+    _shape(q_w, "q_w", (hd,))
+    _shape(k_w, "k_w", (hd,))
     m = {"rope": _lib.BEAM_QK_ROPE, "ssmax": _lib.BEAM_QK_SSMAX}[mode]
     tab, max_pos = 0, 0
+    ops = dict(q=q, k=k, q_w=q_w, k_w=k_w, pos=pos)
     if mode == "rope":
         _check(rope_table, "rope_table", torch.float32, 2)
+        if rope_table.shape[1] != hd:
+            raise ValueError(f"rope_table must be [max_pos, {hd}] (cos | sin)")
         tab, max_pos = rope_table.data_ptr(), rope_table.shape[0]
+        ops["rope_table"] = rope_table
+    _on_current_device(**ops)
     st = _lib.load().beam_qk_norm_ex(_stream_ptr(stream), q.data_ptr(), k.data_ptr(), q_w.data_ptr(),
                                      k_w.data_ptr(), pos.data_ptr(), tab or None, max_pos, T,
                                      q.shape[1], k.shape[1], q.shape[2], float(eps), m,
