@@ -463,16 +463,24 @@ int oracle_qk_norm(bf16_t* q, bf16_t* k, const bf16_t* qw, const bf16_t* kw, con
  *   0, 0.5, 1, 1.5, 2, 3, 4, 6), two per byte, element 2i in the low nibble;
  *   one FP8 E4M3 (OCP E4M3FN, bias 7, largest 448) scale per 16 consecutive
  *   elements; an FP32 global scale gs from the caller.
- * Per block of the BF16 row y:
+ * The steps of a block are those of TensorRT-LLM's open-source FP4 quantiser
+ * (which vLLM and SGLang reuse for NVFP4 activations): the block scale is
+ * gs * (amax / 6) rounded to E4M3, and every value is multiplied by one
+ * per-block FP32 factor, the reciprocal of (E4M3 scale / gs), before its
+ * saturating nearest-even E2M1 conversion. That code forms the factor from
+ * hardware reciprocal approximations; this reading takes each step as one
+ * correctly rounded FP32 operation. Per block of the BF16 row y:
  *   amax = max |y_j|
  *   sf   = E4M3(RN32(RN32(amax / 6) * gs))           nearest, ties to even, saturating
- *   inv  = RN32(gs / sf)                              one division per block
+ *   inv  = RN32(gs / sf)                              one factor per block
  *   q_j  = sf == 0 ? +0 : E2M1(RN32(y_j * inv))
  * Both conversions are written out as a nearest search over the format's
  * finite values (ties to the even code, magnitudes above the largest value,
  * infinities included, saturate; the sign is kept). A NaN converts to E4M3's
- * NaN code 0x7F; E2M1 has no NaN, and a NaN converts to +6 (code 0x7), as
- * NVIDIA's saturating conversion does. The block amax skips NaN values.
+ * NaN code 0x7F. E2M1 has no NaN and neither the pages nor the recipe say
+ * what a NaN becomes; the reading sends it to the largest code, +6 (0x7), as
+ * saturation does with every value beyond the finite range. The block amax
+ * skips NaN values (a maximum ignores them).
  * ---------------------------------------------------------------------- */
 
 static float e4m3_value(unsigned code) { /* finite codes 0..0x7E of the magnitude */

@@ -92,6 +92,9 @@ MUTANTS = [
     ("FP8/FP4 saturation left to the distance search",
      "    if (mag >= value(n_codes - 1)) return n_codes - 1;\n", ""),
     ("NVFP4 block max takes NaN", "if (a > amax) amax = a;", "if (!(a <= amax)) amax = a;"),
+    ("NVFP4 per-element division instead of one reciprocal factor per block",
+     "float a = oracle_bf16_to_f32(y[blk * 16 + j]) * inv;\n                float b = oracle_bf16_to_f32(y[blk * 16 + j + 1]) * inv;",
+     "float a = (oracle_bf16_to_f32(y[blk * 16 + j]) * gs) / sv;\n                float b = (oracle_bf16_to_f32(y[blk * 16 + j + 1]) * gs) / sv;"),
     ("E2M1 NaN encoded as zero", "    if (isnan(v)) return 0x7;\n", "    if (isnan(v)) return 0x0;\n"),
     ("routing keeps one group too many", "for (int k = 0; k < topk_group; ++k) {",
      "for (int k = 0; k <= topk_group && k < n_group; ++k) {"),

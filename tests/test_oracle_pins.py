@@ -778,6 +778,30 @@ def test_nvfp4_hand_block():
     assert sf[0] == 0 and not q.any()
 
 
+def _load_nvfp4_golden():
+    vals = {}
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "nvfp4_reciprocal_scale.txt")):
+        if line.startswith("#") or ":" not in line:
+            continue
+        k, v = line.split(":", 1)
+        vals[k.strip()] = v.split()
+    return vals
+
+
+def test_nvfp4_block_scale_is_one_reciprocal_factor_per_block():
+    # hand-worked block (tests/golden/nvfp4_reciprocal_scale.txt): every value is
+    # multiplied by inv = RN32(gs / sf); dividing each RN32(y * gs) by sf instead
+    # gives other codes on six of the sixteen values
+    g = _load_nvfp4_golden()
+    gs = float(np.array([int(g["gs_bits"][0], 16)], np.uint32).view(np.float32)[0])
+    y = np.array([float(v) for v in g["y"]], np.float32)
+    q, sf = oracle.nvfp4_row(bf16_bits(y), gs)
+    assert int(sf[0]) == int(g["sf_code"][0], 16)
+    nib = [int(q[i // 2]) >> (4 * (i % 2)) & 0xF for i in range(16)]
+    assert nib == [int(c) for c in g["codes"]]
+    assert nib != [int(c) for c in g["per_element_codes"]]
+
+
 def test_nvfp4_dequantises_within_half_a_step():
     rng = np.random.default_rng(91)
     y = bf16_bits(rng.standard_normal(5120) * 2)
