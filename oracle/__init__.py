@@ -100,6 +100,10 @@ def _load():
             lib.oracle_route.restype = i32
             lib.oracle_sigmoid.argtypes = [f32]
             lib.oracle_sigmoid.restype = f32
+            lib.oracle_sigmoid_array.argtypes = [vp, vp, i64]
+            lib.oracle_sigmoid_array.restype = None
+            lib.oracle_sigmoid_undecided.argtypes = []
+            lib.oracle_sigmoid_undecided.restype = ctypes.c_ulonglong
             _lib = lib
     return _lib
 
@@ -264,6 +268,27 @@ def residual_ld(h, x, n: int) -> np.ndarray:
 
 def sigmoid(z: float) -> float:
     return float(_load().oracle_sigmoid(z))
+
+
+def sigmoid_array(z, threads: int = 1) -> np.ndarray:
+    """The router sigmoid of every element of a float32 array (row-parallel over threads)."""
+    z = np.ascontiguousarray(z, dtype=np.float32).ravel()
+    s = np.empty_like(z)
+    lib = _load()
+    if threads <= 1 or z.size < 1 << 16:
+        lib.oracle_sigmoid_array(_p(z), _p(s), z.size)
+        return s
+    step = -(-z.size // threads)
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda lo: lib.oracle_sigmoid_array(_p(z[lo:lo + step]), _p(s[lo:lo + step]),
+                                                         min(step, z.size - lo)),
+                    range(0, z.size, step)))
+    return s
+
+
+def sigmoid_undecided() -> int:
+    """Sigmoid evaluations that neither precision level decided (expected: 0)."""
+    return int(_load().oracle_sigmoid_undecided())
 
 
 def route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8,

@@ -51,6 +51,7 @@
  * The *_ld functions repeat the boundary in long double with no rounding at
  * all; they exist for the hand-worked and closed-form checks.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -316,18 +317,115 @@ void oracle_residual_ld(long double* h, const long double* x, int n, int64_t cou
  *
  * Per token, FP32 throughout:
  *   s_e = RN32(1 / (1 + exp(-z_e)))       the sigmoid, correctly rounded
- *                                         (evaluated in double, rounded once)
  *   b_e = RN32(s_e + bias_e)              biased score, used only to choose
  *   group score = RN32(top1 + top2) of the b_e in the group (the pages say the
  *                 routing matches DeepSeek-V3, whose group score is the sum of
  *                 the group's two best biased scores)
  *   keep the topk_group best groups; among their experts take the topk best
- *   b_e. Ties go to the lower index; the output is in descending b_e.
+ *   b_e. Ties go to the lower index; the output is in descending b_e. A NaN
+ *   score (the pages do not speak of one) ranks below every number, NaNs
+ *   among themselves by index: one total order, so exactly topk_group groups
+ *   and topk experts are kept whatever the inputs hold.
  *   sum = RN32 running sum of the chosen s_e in output order
  *   w_k = RN32(RN32(s_k / sum) * scale)
+ *
+ * The sigmoid is the FP32 value nearest to 1 / (1 + e^-z), found by Ziv's
+ * strategy (A. Ziv, "Fast evaluation of elementary mathematical functions
+ * with correctly rounded last bit", ACM TOMS 17(3), 1991): evaluate with a
+ * known error bound and accept the rounding when every value within the bound
+ * rounds alike; otherwise evaluate again with more precision. Each level
+ * forms the value as hi + lo:
+ *   |z| >= 2^-4: hi = 1/(1+e) for z >= 0, e/(1+e) for z < 0, e = e^-|z|
+ *                (lo = 0); exp within 1 ulp, then one add and one division:
+ *                within 3 ulps of the exact value, relative.
+ *   |z| <  2^-4: hi = 1/2, lo = tanh(z/2)/2 (sigma(z) = (1 + tanh(z/2))/2),
+ *                tanh within a few ulps of lo. Near 0 the value sits within
+ *                z^3/48 of 1/2 + z/4, which is a rounding midpoint for every
+ *                z that is an odd multiple of 2^-23 (2^-24 below zero); a
+ *                bound relative to lo, not to the value, decides those.
+ *   level 1: double, accepted with the bound 2^-49 relative to hi or lo;
+ *   level 2: long double (64 or 113 significant bits), bound 2^-(p-4).
+ * For z != 0 the exact value is transcendental (Lindemann-Weierstrass), so
+ * it never sits on a rounding midpoint and some precision always decides; a
+ * value that level 2 still leaves open is counted (oracle_sigmoid_undecided)
+ * and the tests require that count to stay 0.
  * ---------------------------------------------------------------------- */
 
-static float sigmoid_rn32(float z) { return (float)(1.0 / (1.0 + exp(-(double)z))); }
+static unsigned long long g_sigmoid_undecided;
+
+/* 1 when every value of [hi + lo - eb, hi + lo + eb] rounds to the same
+ * binary32 value *out. The candidates are RN32(hi + lo) and its two
+ * neighbours (hi + lo rounded first may fall on a midpoint that the exact
+ * sum does not reach). The midpoints between neighbouring floats are exact in
+ * double; hi - midpoint is exact (Sterbenz) and adding lo and eb keeps its
+ * sign, so each comparison is decided correctly. */
+static int rn32_certain(double hi, double lo, double eb, float* out) {
+    const float f0 = (float)(hi + lo);
+    const float cand[3] = {f0, nextafterf(f0, -INFINITY), nextafterf(f0, INFINITY)};
+    *out = f0;
+    for (int i = 0; i < 3; ++i) {
+        const float f = cand[i];
+        const double m_lo = 0.5 * ((double)f + (double)nextafterf(f, -INFINITY));
+        const double m_hi = 0.5 * ((double)f + (double)nextafterf(f, INFINITY));
+        if (((hi - m_lo) + lo) - eb > 0.0 && ((hi - m_hi) + lo) + eb < 0.0) {
+            *out = f;
+            return 1;
+        }
+    }
+    return 0;
+}
+
+static int rn32_certain_l(long double hi, long double lo, long double eb, float* out) {
+    const float f0 = (float)(hi + lo);
+    const float cand[3] = {f0, nextafterf(f0, -INFINITY), nextafterf(f0, INFINITY)};
+    *out = f0;
+    for (int i = 0; i < 3; ++i) {
+        const float f = cand[i];
+        const long double m_lo = 0.5L * ((long double)f + (long double)nextafterf(f, -INFINITY));
+        const long double m_hi = 0.5L * ((long double)f + (long double)nextafterf(f, INFINITY));
+        if (((hi - m_lo) + lo) - eb > 0.0L && ((hi - m_hi) + lo) + eb < 0.0L) {
+            *out = f;
+            return 1;
+        }
+    }
+    return 0;
+}
+
+static float sigmoid_rn32(float z) {
+    if (isnan(z)) return z;
+    float r;
+    const int small = fabsf(z) < 0x1p-4f;
+    {
+        double hi = 0.5, lo = 0.0;
+        if (small) {
+            lo = 0.5 * tanh(0.5 * (double)z);
+        } else {
+            const double e = exp(-fabs((double)z));
+            hi = z >= 0.0f ? 1.0 / (1.0 + e) : e / (1.0 + e);
+        }
+        if (rn32_certain(hi, lo, ldexp(small ? fabs(lo) : hi, -49) + 0x1p-1070, &r)) return r;
+    }
+    {
+        long double hi = 0.5L, lo = 0.0L;
+        if (small) {
+            lo = 0.5L * tanhl(0.5L * (long double)z);
+        } else {
+            const long double e = expl(-fabsl((long double)z));
+            hi = z >= 0.0f ? 1.0L / (1.0L + e) : e / (1.0L + e);
+        }
+        if (rn32_certain_l(hi, lo, ldexpl(small ? fabsl(lo) : hi, 4 - LDBL_MANT_DIG) + 0x1p-1070L, &r))
+            return r;
+    }
+    __atomic_fetch_add(&g_sigmoid_undecided, 1ull, __ATOMIC_RELAXED);
+    return r;
+}
+
+/* a ranks before b: a larger number, or a number against a NaN; equal values
+ * (and two NaNs) are left to the index */
+static int score_before(float a, float b) {
+    if (isnan(a)) return 0;
+    return isnan(b) || a > b;
+}
 
 /* index of the best of the first n values of v whose taken[] flag is 0
  * (ties: the lower index); -1 if none */
@@ -335,7 +433,7 @@ static int best_free(const float* v, const unsigned char* taken, int n) {
     int best = -1;
     for (int i = 0; i < n; ++i) {
         if (taken[i]) continue;
-        if (best < 0 || v[i] > v[best]) best = i;
+        if (best < 0 || score_before(v[i], v[best])) best = i;
     }
     return best;
 }
@@ -393,6 +491,14 @@ int oracle_route(const float* logits, const float* bias, int64_t T, int E, int n
 
 /* the FP32 sigmoid the router uses, exposed for the pins */
 float oracle_sigmoid(float z) { return sigmoid_rn32(z); }
+
+/* the same over an array (tests compare whole ranges of inputs) */
+void oracle_sigmoid_array(const float* z, float* s, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) s[i] = sigmoid_rn32(z[i]);
+}
+
+/* sigmoid values that the two precision levels left undecided (none are expected) */
+unsigned long long oracle_sigmoid_undecided(void) { return __atomic_load_n(&g_sigmoid_undecided, __ATOMIC_RELAXED); }
 
 /* ------------------------------------------------------------------------
  * Per-head Q/K RMSNorm with RoPE or SSMax (vLLM page, "Beam model

@@ -67,8 +67,8 @@ MUTANTS = [
      "        if (best < 0 || v[i] >= v[best]) best = i;"),
     ("routing weights not renormalised", "            float q = s[id[k]] / sum;", "            float q = s[id[k]];"),
     ("routing scale not applied", "            w_out[t * topk + k] = q * scale;", "            w_out[t * topk + k] = q;"),
-    ("routing sigmoid of the wrong sign", "static float sigmoid_rn32(float z) { return (float)(1.0 / (1.0 + exp(-(double)z))); }",
-     "static float sigmoid_rn32(float z) { return (float)(1.0 / (1.0 + exp((double)z))); }"),
+    ("routing sigmoid of the wrong sign", "hi = z >= 0.0f ? 1.0 / (1.0 + e) : e / (1.0 + e);",
+     "hi = z >= 0.0f ? e / (1.0 + e) : 1.0 / (1.0 + e);"),
     ("RoPE pairs neighbours instead of halves",
      "float a = oracle_bf16_to_f32(vn[j]), b = oracle_bf16_to_f32(vn[j + 64]);",
      "float a = oracle_bf16_to_f32(vn[j]), b = oracle_bf16_to_f32(vn[(j + 1) % 128]);"),
@@ -98,6 +98,13 @@ MUTANTS = [
     ("E2M1 NaN encoded as zero", "    if (isnan(v)) return 0x7;\n", "    if (isnan(v)) return 0x0;\n"),
     ("routing keeps one group too many", "for (int k = 0; k < topk_group; ++k) {",
      "for (int k = 0; k <= topk_group && k < n_group; ++k) {"),
+    ("router sigmoid without the split form near 0",
+     "const int small = fabsf(z) < 0x1p-4f;", "const int small = 0;"),
+    ("router sigmoid rounding test without the neighbouring candidates",
+     "for (int i = 0; i < 3; ++i) {", "for (int i = 0; i < 1; ++i) {"),
+    ("routing ranks a NaN score first",
+     "    if (isnan(a)) return 0;\n    return isnan(b) || a > b;",
+     "    if (isnan(a)) return 1;\n    return isnan(b) || a > b;"),
     ("RoPE cross term with the cosine", "bc = b * c, as = a * s;", "bc = b * c, as = a * c;"),
     ("SSMax exponent 0.2", "(double)(pos + 1) / 2048.0, 0.1);", "(double)(pos + 1) / 2048.0, 0.2);"),
     ("E4M3 subnormals one binade low", "ldexpf((float)m / 8.0f, -6)", "ldexpf((float)m / 8.0f, -7)"),

@@ -518,6 +518,27 @@ def test_router_sigmoid_is_the_correctly_rounded_fp32_value():
         assert f32(oracle.sigmoid(float(z))) == _sigmoid_exact_f32(float(z)), z
 
 
+def test_router_sigmoid_next_to_rounding_midpoints_and_at_the_ends():
+    # z = m 2^-23 (and -m 2^-24): 1/2 + z/4 is a float or a rounding midpoint and
+    # the sigmoid lies only about z^3/48 below (above) it, far inside a double's
+    # rounding error; subnormal results below z = -87.3; 0 and 1 at the ends
+    zs = [m * 2.0 ** -23 for m in range(1, 65)] + [-m * 2.0 ** -24 for m in range(1, 65)]
+    zs += [-m * 2.0 ** -23 for m in range(1, 33)] + [m * 2.0 ** -22 for m in range(1, 33)]
+    zs += [-87.5, -90.0, -95.25, -100.0, -103.5, -103.96, -103.98, 16.5, 17.0, 17.33, 17.5, 50.0]
+    for z in zs:
+        z = float(f32(z))
+        assert f32(oracle.sigmoid(z)) == _sigmoid_exact_f32(z), z.hex()
+    assert oracle.sigmoid(0.0) == 0.5 and oracle.sigmoid(-0.0) == 0.5
+    assert oracle.sigmoid(math.inf) == 1.0 and oracle.sigmoid(-math.inf) == 0.0
+    assert oracle.sigmoid(104.0) == 1.0 and oracle.sigmoid(-104.0) == 0.0
+    assert math.isnan(oracle.sigmoid(math.nan))
+    # 3 2^-23: 1/2 + z/4 = 1/2 + 1.5 2^-24 is the midpoint of 1/2 + 2^-24 and
+    # 1/2 + 2^-23 (a tie would go to the latter, the even one); the sigmoid is
+    # about 2^-71 below it, so it rounds down
+    assert oracle.sigmoid(3 * 2.0 ** -23) == 0.5 + 2.0 ** -24
+    assert oracle.sigmoid_undecided() == 0
+
+
 def _route_inputs(T, E, seed, bias_scale=0.1):
     rng = np.random.default_rng(seed)
     z = (rng.standard_normal((T, E)) * 2).astype(np.float32)
@@ -584,6 +605,31 @@ def test_routing_hand_example_with_a_group_tie():
     s1 = oracle.sigmoid(2.0)
     assert idx.tolist() == [[0, 1]]
     assert w[0, 0] == f32(f32(0.5) / f32(0.5 + s1)) and w[0, 0] < w[0, 1]
+
+
+def test_routing_ranks_nan_scores_below_every_number():
+    # E = 8 in two groups of 4, z = 0 (every sigmoid 1/2) unless NaN; a NaN
+    # logit gives a NaN score, which ranks after every number (NaNs among
+    # themselves by index)
+    b = np.array([0, 0.5, 0, 0, 0.25, 0.5, 0.25, 0], np.float32)
+    # group 0 biased 0.5 NaN 0.5 0.5 -> 1.0; group 1: 0.75 1.0 0.75 0.5 -> 1.75
+    z = np.zeros((1, 8), np.float32)
+    z[0, 1] = np.nan
+    idx, w = oracle.route(z, b, n_group=2, topk_group=1, topk=2, scale=1.0)
+    assert idx.tolist() == [[5, 4]] and w.tolist() == [[0.5, 0.5]]
+    # group 0: 0.5 1.0 0.5 0.5 -> 1.5; group 1: NaN 1.0 0.75 0.5 -> 1.75
+    z = np.zeros((1, 8), np.float32)
+    z[0, 4] = np.nan
+    idx, w = oracle.route(z, b, n_group=2, topk_group=1, topk=2, scale=1.0)
+    assert idx.tolist() == [[5, 6]]
+    # group 1 all NaN: its score is NaN and group 0 is kept; with both groups
+    # kept, the NaN experts come after every number, lowest index first
+    z = np.zeros((1, 8), np.float32)
+    z[0, 4:] = np.nan
+    idx, w = oracle.route(z, b, n_group=2, topk_group=1, topk=3, scale=1.0)
+    assert idx.tolist() == [[1, 0, 2]]
+    idx, w = oracle.route(z, b, n_group=2, topk_group=2, topk=6, scale=1.0)
+    assert idx.tolist() == [[1, 0, 2, 3, 4, 5]] and np.isnan(w).all()
 
 
 def test_scaled_combine_by_a_power_of_two_equals_prescaled_weights():
