@@ -101,6 +101,71 @@ def shard_rows(total: int, rank: int, world: int) -> tuple[int, int]:
 
 # ------------------------------------------------------------------ clocks
 
+class NvmlClockSampler:
+    """SM clock, its maximum and the clock event (throttle) reasons, polled through
+    NVML (libnvidia-ml, query calls only: nothing is set) every ~1 ms from a thread,
+    so that a timed region of a few milliseconds still holds samples."""
+    NAMES = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+             0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_id: str | None, index: int):
+        import ctypes
+        self.rows: list[tuple[float, float, float, int]] = []
+        self.ok = False
+        self._stop = threading.Event()
+        self.t = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            rc = (lib.nvmlDeviceGetHandleByUUID(gpu_id.encode(), ctypes.byref(h)) if gpu_id
+                  else lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)))
+            if rc != 0:
+                return
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.lib, self.h, self.ct = lib, h, ctypes
+            self.ok = self._poll() is not None
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _poll(self):
+        ct = self.ct
+        mhz, mx, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        if (self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) != 0 or  # NVML_CLOCK_SM
+                self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx)) != 0 or
+                self.reasons_fn(self.h, ct.byref(rs)) != 0):
+            return None
+        return float(mhz.value), float(mx.value), int(rs.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            r = self._poll()
+            if r is not None:
+                self.rows.append((time.time(),) + r)
+            time.sleep(0.001)
+
+    def start(self):
+        self.t = threading.Thread(target=self._run, daemon=True)
+        self.t.start()
+
+    def stop(self):
+        self._stop.set()
+        if self.t:
+            self.t.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [r for r in self.rows if t0 <= r[0] <= t1]
+        mhz = sorted(r[1] for r in inside)
+        reasons = set()
+        for r in inside:
+            reasons |= {n for bit, n in self.NAMES.items() if r[3] & bit}
+        return {"sm_mhz": mhz[len(mhz) // 2] if mhz else None,
+                "sm_max_mhz": inside[-1][2] if inside else None, "reasons": sorted(reasons),
+                "samples": len(inside), "source": "nvml, ~1 ms polling"}
+
+
 class ClockSampler:
     QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -325,12 +390,12 @@ def route_bytes(T: int) -> int:
     return T * (256 * 4 + 8 * 8) + 256 * 4   # FP32 logits in; ids and weights out; bias
 
 
-def _time_launches(fn, stream, reps: int, warmup: int = 3) -> float:
-    """Mean microseconds per launch, CUDA events on the launching stream."""
+MIN_LAUNCHES, MIN_SECONDS = 1000, 0.5
+
+
+def _time_loop(fn, stream, reps: int) -> float:
     import torch
     with torch.cuda.stream(stream):
-        for i in range(warmup):
-            fn(i)
         a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for i in range(reps):
@@ -338,6 +403,22 @@ def _time_launches(fn, stream, reps: int, warmup: int = 3) -> float:
         e.record(stream)
     torch.cuda.synchronize()
     return a.elapsed_time(e) * 1e3 / reps
+
+
+def _time_launches(fn, stream, reps: int | None = None, warmup: int = 3) -> tuple[float, int]:
+    """Mean microseconds per launch over back-to-back launches, CUDA events on the
+    launching stream: `reps` launches, or by default at least MIN_LAUNCHES and at
+    least MIN_SECONDS of launches (sized from a 20-launch estimate). Returns
+    (us, launches)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fn(i)
+    torch.cuda.synchronize()
+    if reps is None:
+        est = _time_loop(fn, stream, 20)
+        reps = max(MIN_LAUNCHES, int(MIN_SECONDS / (est * 1e-6)) + 1)
+    return _time_loop(fn, stream, reps), reps
 
 
 def next_rows(snr, device, dev, peak: float, sm_mhz: float | None = None) -> dict:
@@ -363,9 +444,10 @@ def next_rows(snr, device, dev, peak: float, sm_mhz: float | None = None) -> dic
     b = torch.from_numpy(synth.normal(3, 9, 256) * 0.05).to(device)
     idx = torch.empty((T, 8), dtype=torch.int32, device=device)
     w = torch.empty((T, 8), dtype=torch.float32, device=device)
-    us = _time_launches(lambda i: snr.moe_route(z[i % nbuf], b, idx=idx, w=w, stream=stream),
-                        stream, 50)
+    us, n_rt = _time_launches(lambda i: snr.moe_route(z[i % nbuf], b, idx=idx, w=w, stream=stream),
+                              stream)
     rt = entry(us, route_bytes(T))
+    rt["launches"] = n_rt
     if sm_mhz and ROUTE_ISSUE["source_sha"] == kernel_source_sha():
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         issue_peak = sms * 4 * sm_mhz * 1e6  # warp-instructions per second
@@ -387,10 +469,10 @@ def next_rows(snr, device, dev, peak: float, sm_mhz: float | None = None) -> dic
     ang = torch.arange(QK_SEQ, dtype=torch.float64)[:, None] * inv[None, :]
     table = torch.cat([ang.cos(), ang.sin()], 1).float().to(device).contiguous()
     for mode in ("rope", "ssmax"):
-        us = _time_launches(lambda i, mode=mode: snr.qk_norm(
+        us, nl = _time_launches(lambda i, mode=mode: snr.qk_norm(
             q, k, qw, kw, pos, 1e-6, mode=mode, rope_table=table if mode == "rope" else None,
-            stream=stream), stream, 20)
-        out[f"qk_norm_{mode}"] = entry(us, qk_bytes(T, mode == "rope"))
+            stream=stream), stream)
+        out[f"qk_norm_{mode}"] = dict(entry(us, qk_bytes(T, mode == "rope")), launches=nl)
     del q, k
 
     # the boundaries with y as NVFP4, on the step's own buffers
@@ -398,14 +480,14 @@ def next_rows(snr, device, dev, peak: float, sm_mhz: float | None = None) -> dic
     gs = 336.0
     yq = torch.empty((T, D // 2), dtype=torch.uint8, device=device)
     ys = torch.empty((T, D // 16), dtype=torch.uint8, device=device)
-    us = _time_launches(lambda i: snr.boundary_fused_nvfp4(
+    us, nl = _time_launches(lambda i: snr.boundary_fused_nvfp4(
         dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, gs, y_fp4=yq, y_scale=ys,
-        stream=stream), stream, 20)
-    out["dense_boundary_nvfp4"] = entry(us, nvfp4_bytes(T, False))
-    us = _time_launches(lambda i: snr.moe_combine_boundary_nvfp4(
+        stream=stream), stream)
+    out["dense_boundary_nvfp4"] = dict(entry(us, nvfp4_bytes(T, False)), launches=nl)
+    us, nl = _time_launches(lambda i: snr.moe_combine_boundary_nvfp4(
         mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"], mo["pre_w"], MOE_N, EPS, gs,
-        y_fp4=yq, y_scale=ys, stream=stream), stream, 20)
-    out["moe_boundary_nvfp4"] = entry(us, nvfp4_bytes(T, True))
+        y_fp4=yq, y_scale=ys, stream=stream), stream)
+    out["moe_boundary_nvfp4"] = dict(entry(us, nvfp4_bytes(T, True)), launches=nl)
     snr.sync_status(stream)
     return out
 
@@ -429,8 +511,8 @@ def moe_stress(snr, device, peak: float, reps: int = 5) -> dict:
     qw = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["pre_w"], D, 0, 0.1, 1.0)).to(device)
     y = torch.empty_like(h)
     stream = torch.cuda.Stream(device)
-    us = _time_launches(lambda i: snr.moe_combine_boundary(h, e, w, pw, qw, cfg.n, cfg.eps, y=y,
-                                                           stream=stream), stream, reps, warmup=2)
+    us, _ = _time_launches(lambda i: snr.moe_combine_boundary(h, e, w, pw, qw, cfg.n, cfg.eps, y=y,
+                                                              stream=stream), stream, reps, warmup=2)
     snr.sync_status(stream)
     nbytes = T * (22 * D + 32) + 4 * D
     gbs = nbytes / (us * 1e-6) / 1e9
@@ -466,7 +548,9 @@ def bench_ours(args, rank, world, local_rank):
         gpu_id = f"GPU-{uuid}" if uuid and not uuid.startswith("GPU-") else (uuid or None)
     except Exception:
         gpu_id = None
-    sampler = ClockSampler(gpu_id)
+    sampler = NvmlClockSampler(gpu_id, local_rank)
+    if not sampler.ok:
+        sampler = ClockSampler(gpu_id)
     sampler.start()
     time.sleep(0.3)
 
@@ -485,29 +569,18 @@ def bench_ours(args, rank, world, local_rank):
     snr.sync_status(stream)
 
     # per-kernel durations, for the roofline: each kernel alone, back to back on
-    # the launching stream (plain launches), CUDA events around the whole loop
+    # the launching stream (plain launches), CUDA events around the whole loop;
+    # at least MIN_LAUNCHES launches and MIN_SECONDS whatever --steps is
     dn, mo = dev["dense"], dev["moe"]
-    kernel_steps = max(20, min(args.steps, 1000))
-
-    def per_launch_us(launch) -> float:
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                launch()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(kernel_steps):
-                launch()
-            b.record(stream)
-        torch.cuda.synchronize(device)
-        return a.elapsed_time(b) * 1e3 / kernel_steps
-
-    dense_us = per_launch_us(lambda: snr.boundary_fused(
-        dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, y=dn["y"], stream=stream))
-    moe_us = per_launch_us(lambda: snr.moe_combine_boundary(
+    k0 = time.time()
+    dense_us, dense_n = _time_launches(lambda i: snr.boundary_fused(
+        dn["h"], dn["x"], dn["post_w"], dn["pre_w"], DENSE_N, EPS, y=dn["y"], stream=stream), stream)
+    moe_us, moe_n = _time_launches(lambda i: snr.moe_combine_boundary(
         mo["h"], mo["expert_out"], mo["topk_w"], mo["post_w"], mo["pre_w"], MOE_N, EPS, y=mo["y"],
-        stream=stream))
+        stream=stream), stream)
+    k1 = time.time()
     snr.sync_status(stream)
-    time.sleep(0.2)
+    time.sleep(0.05)
     sampler.stop()
 
     ms_total = start.elapsed_time(end)
@@ -577,6 +650,7 @@ def bench_ours(args, rank, world, local_rank):
     tr = NCU_TRAFFIC.get("moe")
     traffic = tr["bytes_per_launch"] if tr and tr.get("source_sha") == sha else None
     clocks = sampler.summary(t0, t1)
+    clocks["per_kernel_loops"] = sampler.summary(k0, k1)
     line = {
         "metric": METRIC,
         "value": world * T_TOKENS / (ms_step * 1e-3),
@@ -597,7 +671,8 @@ def bench_ours(args, rank, world, local_rank):
             "step": ("dense then MoE boundary per step, programmatic dependent launches (each "
                      "kernel stages its weights while the previous one finishes)" if pdl else
                      "dense then MoE boundary per step, plain launches"),
-            "per_kernel": f"each kernel alone, {kernel_steps} back-to-back plain launches, CUDA events",
+            "per_kernel": (f"each kernel alone, back-to-back plain launches (at least {MIN_LAUNCHES} "
+                           f"and {MIN_SECONDS} s: dense {dense_n}, MoE {moe_n}), CUDA events"),
             "dense": {"us": dense_us, "tokens_per_s": T_TOKENS / (dense_us * 1e-6),
                       "GBps": dense_gbs, "frac_of_measured_hbm": dense_gbs / peak,
                       "frac_of_nominal_8TBps": dense_gbs / NOMINAL_HBM_GBS, "bytes": db},

@@ -164,15 +164,29 @@ BEAM_API beam_status beam_moe_combine_boundary_scaled(beam_stream_t stream, uint
  *   topk     in [1, BEAM_ROUTE_MAX_TOPK] and at most topk_group * E / n_group (Beam: 8)
  *   topk_idx [T, topk] int32 expert ids, topk_w [T, topk] FP32; 4-byte aligned,
  *            overlapping neither each other nor the inputs
- * Logits must not be NaN (the choice among NaN scores is unspecified).
- * exp is CUDA's FP32 expf, so s_e may differ from the correctly rounded
- * sigmoid by a few ulps, and an exact tie between two biased scores may then
- * break the other way. Below a logit of about -88.7, expf(-logit) overflows
- * and s_e is 0, where the correctly rounded value is a subnormal under 3e-39.
+ * s_e is the correctly rounded FP32 sigmoid (see beam_router_sigmoid), so the
+ * chosen experts and the weights are the exact FP32 results of these steps.
+ * Scores are ranked on one total order: larger first, a NaN score below every
+ * number, equal scores (and NaNs) by index; so exactly topk experts from
+ * exactly topk_group groups are chosen whatever the logits and bias hold.
  */
 BEAM_API beam_status beam_moe_route(beam_stream_t stream, const float* logits, const float* bias,
                                     int64_t T, int E, int n_group, int topk_group, int topk,
                                     float route_scale, int32_t* topk_idx, float* topk_w);
+
+/*
+ * The router's FP32 sigmoid alone, elementwise (vLLM page, "MoE and residual
+ * stream": expert scores are the sigmoid of the router logits; SGLang page,
+ * "Dense layers and grouped MoE routing": FP32 routing). s[i] is the float
+ * nearest 1 / (1 + e^-z[i]), the exact sigmoid rounded once to nearest-even,
+ * for every float input: +-0 -> 0.5, +inf -> 1, -inf -> +0, NaN -> NaN, and a
+ * subnormal where the value is one. beam_moe_route scores with this same
+ * function.
+ *   z, s   [count] FP32 device arrays, 4-byte aligned; s may be z itself
+ *          (in place) but must not overlap it otherwise
+ *   count  >= 0 (0 launches nothing)
+ */
+BEAM_API beam_status beam_router_sigmoid(beam_stream_t stream, const float* z, float* s, int64_t count);
 
 /* Head dimension and modes of beam_qk_norm. */
 #define BEAM_QK_HEAD_DIM 128
@@ -253,10 +267,12 @@ typedef struct {
 /* Take the exact integer row-sum path for every row instead of only for rows
  * whose compensated sum cannot be certified (results are identical). */
 #define BEAM_OPT_FORCE_EXACT_SUM 0x1u
-/* Test hook for the bounded waits (dense boundary, ring kernel only): every CTA
- * first waits on an mbarrier that nothing completes; the wait gives up after
- * 1 ms, the device status word records it (beam_sync_status then returns
- * BEAM_ERR_TIMEOUT) and the launch carries on normally. */
+/* Test hook for the bounded waits (dense boundary, ring kernel only): the bulk
+ * copy of each CTA's second row is never issued, so the wait for that row gives
+ * up after 1 ms. The CTA then stores nothing for that row or its later rows
+ * (h and y keep what they held), waits for its copies in flight and returns;
+ * the device status word records it and beam_sync_status returns
+ * BEAM_ERR_TIMEOUT. Each CTA's first row is computed as usual. */
 #define BEAM_OPT_TEST_WAIT_TIMEOUT 0x2u
 /* Programmatic dependent launch (the following norm loads its weights before
  * its dependency wait: SGLang page, "Fusion optimizations"). The kernel may

@@ -17,7 +17,7 @@ from ._lib import LaunchOpts  # noqa: F401
 
 __all__ = ["boundary_fused", "moe_combine_boundary", "boundary_fused_host",
            "moe_combine_boundary_host", "boundary_fused_nvfp4",
-           "moe_combine_boundary_nvfp4", "moe_route", "qk_norm", "sync_status",
+           "moe_combine_boundary_nvfp4", "moe_route", "router_sigmoid", "qk_norm", "sync_status",
            "exact_sum_count",
            "version", "BeamError", "LaunchOpts", "library"]
 
@@ -321,6 +321,24 @@ def moe_route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8
     if st != 0:
         raise BeamError(st, "beam_moe_route")
     return idx, w
+
+
+def router_sigmoid(z, out=None, stream=None):
+    """The router's correctly rounded FP32 sigmoid of every element of ``z`` (float32 CUDA
+    tensor, any shape, contiguous); ``out`` may be ``z`` (in place)."""
+    import torch
+    if not isinstance(z, torch.Tensor) or z.dtype != torch.float32 or not z.is_contiguous():
+        raise TypeError("z must be a contiguous float32 tensor")
+    if out is None:
+        out = torch.empty_like(z)
+    if not isinstance(out, torch.Tensor) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise TypeError("out must be a contiguous float32 tensor")
+    _shape(out, "out", tuple(z.shape))
+    _on_current_device(z=z, out=out)
+    st = _lib.load().beam_router_sigmoid(_stream_ptr(stream), z.data_ptr(), out.data_ptr(), z.numel())
+    if st != 0:
+        raise BeamError(st, "beam_router_sigmoid")
+    return out
 
 
 def qk_norm(q, k, q_w, k_w, pos, eps: float = 1e-6, mode: str = "rope", rope_table=None,

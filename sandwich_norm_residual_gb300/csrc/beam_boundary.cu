@@ -622,6 +622,24 @@ beam_status beam_moe_route(beam_stream_t stream, const float* logits, const floa
     return BEAM_OK;
 }
 
+beam_status beam_router_sigmoid(beam_stream_t stream, const float* z, float* s, int64_t count) {
+    if (count < 0 || count > (int64_t(1) << 40)) return BEAM_ERR_SHAPE;
+    if (count == 0) return BEAM_OK;
+    if (!z || !s) return BEAM_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(z) & 3u) || (reinterpret_cast<uintptr_t>(s) & 3u)) return BEAM_ERR_ALIGN;
+    const size_t nb = (size_t)count * 4u;
+    if ((const void*)z != (const void*)s && overlaps(z, nb, s, nb)) return BEAM_ERR_ALIAS;
+    DeviceInfo* info = nullptr;
+    beam_status st = current_device(&info);
+    if (st != BEAM_OK) return st;
+    int64_t blocks = (count + 255) / 256;
+    const int64_t cap = (int64_t)info->sms * 8;  // grid-stride beyond 8 blocks per SM
+    if (blocks > cap) blocks = cap;
+    beam::router_sigmoid_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(z, s, count);
+    if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+    return BEAM_OK;
+}
+
 beam_status beam_moe_combine_boundary(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,
                                       const float* topk_w, const uint16_t* post_w, const uint16_t* pre_w, int n,
                                       float eps, int64_t T, int D, uint16_t* y_out) {

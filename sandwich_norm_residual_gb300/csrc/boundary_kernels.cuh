@@ -471,11 +471,17 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
 // the post-norm reduction's barrier shows every thread has read it, so up to
 // stages-1 rows per CTA are in flight while a row is computed. FULL kernels
 // keep the BF16 weights after the ring.
+//
+// Every slot wait is bounded. The threads vote after each wait: if any wait
+// gave up, the CTA stores nothing for that row or any later row of its own
+// (h and y keep what they held), records the timeout in the device status
+// word, waits (bounded) for the copies it still has in flight, and returns.
+// Test hook (kFlagTestWaitTimeout): the copy of each CTA's second row is never
+// issued, so that row's wait runs out after test_wait_ns.
 template <int VPT, bool FULL>
 __global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const BoundaryParams p) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
-    __shared__ __align__(8) uint64_t test_bar;
     __shared__ RedScratch rs;
     __shared__ ExactScratch sc;
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -483,10 +489,14 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const Bounda
     const uint32_t row_bytes = (uint32_t)p.D * 2u;
     const long long G = gridDim.x;
     const long long n_iter = (p.T - blockIdx.x + G - 1) / G;  // grid <= T: at least one row
+    const bool hook = (p.flags & kFlagTestWaitTimeout) != 0;
+    const unsigned long long wait_ns = hook ? p.test_wait_ns : p.wait_ns;
     uint4* ws = FULL ? reinterpret_cast<uint4*>(ring + (size_t)S * 2u * row_bytes) : nullptr;
 
     auto slot_x = [&](int s) { return ring + (size_t)s * 2u * row_bytes; };
+    auto issued = [&](long long i) { return !(hook && i == 1); };
     auto issue = [&](long long i) {  // thread 0 only
+        if (!issued(i)) return;
         const int s = (int)(i % S);
         const size_t off = (size_t)(blockIdx.x + i * G) * (size_t)p.D;
         mbar_arrive_expect_tx(&full[s], 2u * row_bytes);
@@ -496,7 +506,6 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const Bounda
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
-        mbar_init(&test_bar, 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -506,19 +515,14 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const Bounda
     if (tid == 0)
         for (long long i = 0; i < S && i < n_iter; ++i) issue(i);
 
-    // test hook: wait on a barrier that nothing completes; it must run out
-    if ((p.flags & kFlagTestWaitTimeout) && !mbar_wait_bounded(&test_bar, 0, p.test_wait_ns) && tid == 0)
-        report_timeout();
-
-    bool dead = false;             // a wait of this thread gave up: skip later waits and refills
-    long long dead_from = n_iter;  // first iteration whose copies thread 0 did not see complete
+    long long dead_from = n_iter;  // first row whose wait gave up (n_iter: none)
     for (long long i = 0; i < n_iter; ++i) {
         const int s = (int)(i % S);
         const uint32_t parity = (uint32_t)((i / S) & 1);
-        if (!dead && !mbar_wait_bounded(&full[s], parity, p.wait_ns)) {
-            dead = true;
+        const bool ok = mbar_wait_bounded(&full[s], parity, wait_ns);
+        if (__syncthreads_or(!ok)) {  // block-uniform: every thread leaves the loop here
             dead_from = i;
-            report_timeout();
+            break;
         }
         const uint4* xs = reinterpret_cast<const uint4*>(slot_x(s));
         const uint4* hs = reinterpret_cast<const uint4*>(slot_x(s) + row_bytes);
@@ -530,14 +534,16 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_ring_kernel(const Bounda
             hv[j] = (FULL || vi < p.nvec) ? hs[vi] : make_uint4(0, 0, 0, 0);
         }
         finish_row<VPT, false, FULL, false>(p, blockIdx.x + i * G, xv, hv, &rs, &sc, ws, [&]() {
-            if (tid == 0 && !dead && i + S < n_iter) issue(i + S);
+            if (tid == 0 && i + S < n_iter) issue(i + S);
         });
     }
-    // a slot copy that timed out may still land: wait (bounded) before the
-    // CTA's shared memory is released
-    if (tid == 0 && dead)
+    // after a timeout: the copies issued for rows dead_from .. dead_from + S - 1
+    // may still land; wait for them (bounded) before the shared memory goes
+    if (dead_from < n_iter && tid == 0) {
+        report_timeout();
         for (long long i = dead_from; i < n_iter && i < dead_from + S; ++i)
-            mbar_wait_bounded(&full[i % S], (uint32_t)((i / S) & 1), p.wait_ns);
+            if (issued(i)) mbar_wait_bounded(&full[i % S], (uint32_t)((i / S) & 1), p.wait_ns);
+    }
 }
 
 }  // namespace beam

@@ -2,7 +2,8 @@
 //
 // Per token (vLLM page, "MoE and residual stream"; SGLang page, "Dense layers
 // and grouped MoE routing"), FP32 throughout:
-//   s_e = 1 / (1 + exp(-z_e))        sigmoid of the FP32 router logit
+//   s_e = RN32(1 / (1 + e^-z_e))     sigmoid of the FP32 router logit, the
+//                                    correctly rounded value (router_sigmoid.cuh)
 //   b_e = s_e + bias_e               biased score, used only to choose experts
 //   group score = top1 + top2 of the b_e in the group (the routing matches
 //                 DeepSeek-V3, whose group score is the sum of the group's two
@@ -10,6 +11,9 @@
 //   keep the topk_group best groups, then the topk best experts among them;
 //   ties go to the lower index and the output is in descending b_e
 //   w_k = (s_k / sum_k s_k) * scale, the sum taken in output order
+// Scores are ranked on one total order: larger first, a NaN below every
+// number, equal scores (and NaNs) by index. So exactly topk_group groups and
+// topk experts are chosen whatever the logits and the bias hold.
 //
 // One warp per token; lane l holds experts 8l .. 8l+7 (256 experts), so a group
 // of 256/n_group experts spans 32/n_group neighbouring lanes. Each top-k round
@@ -19,6 +23,8 @@
 #pragma once
 
 #include <cstdint>
+
+#include "router_sigmoid.cuh"
 
 namespace beam {
 
@@ -35,16 +41,19 @@ struct RouteParams {
     float scale;
 };
 
-// (v1, i1) ranks before (v2, i2): larger value, then lower index
-__device__ __forceinline__ bool ranks_before(float v1, int i1, float v2, int i2) {
-    return v1 > v2 || (v1 == v2 && i1 < i2);
-}
-
-// unsigned key that orders like the float (never 0 for a non-NaN value; -0 and
-// +0 differ, but a biased score s + bias is never -0 since s is never -0)
+// unsigned key that orders like the float, with every NaN at 1, below the key
+// of -inf (0x007FFFFF); 0 is left free to mark an unavailable entry. -0 and +0
+// differ, but a biased score s + bias is never -0 since s is never -0, and
+// neither is a sum of two of them.
 __device__ __forceinline__ uint32_t order_key(float v) {
     const uint32_t b = __float_as_uint(v);
+    if (v != v) return 1u;
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// the float of a key (a NaN for key 1)
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 constexpr int kRouteWarps = 8;  // tokens per 256-thread block
@@ -113,7 +122,7 @@ __device__ __forceinline__ void pick_rounds_sorted4(uint32_t (&key)[4], uint32_t
 // per lane and sorted within the lane, which makes each topk round two warp
 // reductions and a shift.
 template <int NG, int TG, int K>
-__global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
+__global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
     constexpr bool kCompact = NG > 0 && TG > 0 && TG * (kRouteExperts / (NG > 0 ? NG : 1)) == 128;
     __shared__ __align__(16) float s_all[kRouteWarps][kRouteExperts];  // unbiased scores, per warp
     const int lane = threadIdx.x & 31;
@@ -130,11 +139,13 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
     const float4 za = __ldg(z4), zb = __ldg(z4 + 1), ba = __ldg(b4), bb = __ldg(b4 + 1);
     const float z[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
     const float bias[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
-    float s[8], b[8];
+    const SigmoidLane lt = sigmoid_lane_table();
+    float s[8];
+    uint32_t bk[8];  // keys of the biased scores
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        s[i] = __frcp_rn(__fadd_rn(1.0f, expf(-z[i])));  // RN(1 / (1 + e)), as a division
-        b[i] = __fadd_rn(s[i], bias[i]);
+        s[i] = router_sigmoid(z[i], lt);
+        bk[i] = order_key(__fadd_rn(s[i], bias[i]));
     }
     float4* mine4 = reinterpret_cast<float4*>(&s_all[warp][8 * lane]);
     mine4[0] = make_float4(s[0], s[1], s[2], s[3]);
@@ -142,31 +153,34 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
 
     // ---- group scores: the sum of the two largest biased scores of each group.
     // Only the two values matter, not which experts hold them, so a running
-    // (largest, second largest) pair of values suffices.
-    float m1 = -INFINITY, m2 = -INFINITY;
+    // (largest, second largest) pair of keys suffices.
+    uint32_t m1 = 0u, m2 = 0u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        m2 = fmaxf(m2, fminf(m1, b[i]));
-        m1 = fmaxf(m1, b[i]);
+        m2 = max(m2, min(m1, bk[i]));
+        m1 = max(m1, bk[i]);
     }
     const int lpg = 32 / n_group;  // lanes per group (a power of two)
 #pragma unroll
     for (int off = 16; off; off >>= 1) {
         if (off >= lpg) continue;
-        const float o1 = __shfl_xor_sync(full, m1, off), o2 = __shfl_xor_sync(full, m2, off);
-        m2 = fmaxf(fminf(m1, o1), fmaxf(m2, o2));
-        m1 = fmaxf(m1, o1);
+        const uint32_t o1 = __shfl_xor_sync(full, m1, off), o2 = __shfl_xor_sync(full, m2, off);
+        m2 = max(min(m1, o1), max(m2, o2));
+        m1 = max(m1, o1);
     }
-    const float gscore = __fadd_rn(m1, m2);
+    // every group has at least 8 experts (n_group <= 32), so m1 and m2 are keys
+    // of real scores
+    const uint32_t gkey = order_key(__fadd_rn(key_value(m1), key_value(m2)));
     const int my_group = lane / lpg;
 
-    // ---- keep the topk_group best groups
+    // ---- keep the topk_group best groups (one total order: exactly
+    // topk_group groups have a rank below topk_group)
     int rank = 0;
 #pragma unroll
     for (int g = 0; g < 32; ++g) {
         if (g >= n_group) break;
-        const float sg = __shfl_sync(full, gscore, g * lpg);
-        rank += ranks_before(sg, g, gscore, my_group) ? 1 : 0;
+        const uint32_t kg = __shfl_sync(full, gkey, g * lpg);
+        rank += (kg > gkey || (kg == gkey && g < my_group)) ? 1 : 0;
     }
     const bool eligible = rank < topk_group;
 
@@ -176,24 +190,26 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
     if constexpr (kCompact) {
         // the 16 lanes of kept groups write their biased scores to slots 0..15
         // in expert order; lane j then holds experts 4j .. 4j+3 of that order
-        __shared__ __align__(16) float ck[kRouteWarps][128];
+        __shared__ __align__(16) uint32_t ck[kRouteWarps][128];
         __shared__ int cb[kRouteWarps][16];
         const unsigned kept = __ballot_sync(full, eligible);
-        if (eligible) {
-            const int slot = __popc(kept & ((1u << (my_group * lpg)) - 1u)) + (lane & (lpg - 1));
-            float4* dst = reinterpret_cast<float4*>(&ck[warp][8 * slot]);
-            dst[0] = make_float4(b[0], b[1], b[2], b[3]);
-            dst[1] = make_float4(b[4], b[5], b[6], b[7]);
+        // exactly 16 lanes are kept (4 whole groups of 4 lanes), so slot < 16;
+        // the bound is checked all the same before the shared-memory writes
+        const int slot = __popc(kept & ((1u << (my_group * lpg)) - 1u)) + (lane & (lpg - 1));
+        if (eligible && slot < 16) {
+            uint4* dst = reinterpret_cast<uint4*>(&ck[warp][8 * slot]);
+            dst[0] = make_uint4(bk[0], bk[1], bk[2], bk[3]);
+            dst[1] = make_uint4(bk[4], bk[5], bk[6], bk[7]);
             cb[warp][slot] = 8 * lane;
         }
         __syncwarp();
-        const float4 v = reinterpret_cast<const float4*>(ck[warp])[lane];
-        uint32_t key[4] = {order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w)};
+        const uint4 v = reinterpret_cast<const uint4*>(ck[warp])[lane];
+        uint32_t key[4] = {v.x, v.y, v.z, v.w};
         pick_rounds_sorted4(key, (uint32_t)(cb[warp][lane >> 1] + 4 * (lane & 1)), topk, lane, sel_i, my_i);
     } else {
         uint32_t key[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) key[i] = eligible ? order_key(b[i]) : 0u;  // 0: unavailable
+        for (int i = 0; i < 8; ++i) key[i] = eligible ? bk[i] : 0u;  // 0: unavailable
         pick_rounds<8>(key, (uint32_t)(8 * lane), topk, lane, sel_i, my_i);
     }
 
@@ -209,6 +225,19 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
     if (lane < topk) {
         p.idx[t * topk + lane] = my_i;
         p.w[t * topk + lane] = __fmul_rn(__fdiv_rn(sw[my_i], sum), p.scale);
+    }
+}
+
+// The router's sigmoid alone, elementwise: s[i] = RN32(1 / (1 + e^-z[i])).
+// Whole warps iterate together (the sigmoid reads its table by shuffle).
+__global__ void __launch_bounds__(256) router_sigmoid_kernel(const float* z, float* s, long long n) {
+    const SigmoidLane lt = sigmoid_lane_table();
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < n; base += stride) {
+        const long long i = base + (threadIdx.x & 31);
+        const float zi = i < n ? z[i] : 0.0f;
+        const float si = router_sigmoid(zi, lt);
+        if (i < n) s[i] = si;
     }
 }
 

@@ -130,37 +130,52 @@ def test_moe_T16384_full():
 
 
 @pytest.mark.slow
-def test_moe_stress_T131072_sampled_rows():
-    """T = 131072 on the GPU in one launch; the oracle checks 1024 sampled rows,
-    half of them tokens with a x100 outlier expert row."""
+def test_moe_stress_T131072_every_row():
+    """T = 131072 on the GPU in one launch, then every row of h' and y against the
+    oracle, row-parallel on the host cores. The 1024 sampled rows (half of them tokens
+    with a x100 expert row) are compared first, as a quick sub-check."""
     cfg = MOE_STRESS_T131072
     T, D, K = cfg.T, cfg.D, cfg.K
-    e = torch.empty((T, K, D), dtype=torch.bfloat16, device=DEV)
+    e_host = torch.empty((T, K, D), dtype=torch.bfloat16)
     chunk = 2048
     for r in range(0, T, chunk):
-        m = min(chunk, T - r)
-        e[r:r + m].copy_(synth.expert_rows(cfg, r, m))
-    h = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["h"], T * D).reshape(T, D)).to(DEV)
-    w = torch.from_numpy(synth.topk_weights(cfg.seed, synth.STREAMS["topk"], T, K,
-                                            cfg.route_scale)).to(DEV)
+        synth.expert_rows(cfg, r, min(chunk, T - r), out=e_host[r:r + chunk])
+    e = e_host.to(DEV)
+    h_host = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["h"], T * D).reshape(T, D))
+    w_host = torch.from_numpy(synth.topk_weights(cfg.seed, synth.STREAMS["topk"], T, K,
+                                                 cfg.route_scale))
     pw = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["post_w"], D, 0, 0.1, 1.0))
     qw = synth.to_bf16(synth.normal(cfg.seed, synth.STREAMS["pre_w"], D, 0, 0.1, 1.0))
-    h_in = h.clone()
-    y = snr.moe_combine_boundary(h, e, w, pw.to(DEV), qw.to(DEV), cfg.n, cfg.eps)
+    h = h_host.to(DEV)
+    y = snr.moe_combine_boundary(h, e, w_host.to(DEV), pw.to(DEV), qw.to(DEV), cfg.n, cfg.eps)
     snr.sync_status()
+    del e
+    h_out, y_out = bits(h), bits(y)
+    del h, y
+
+    def rows_input(idx):
+        return dict(h=h_host[idx], expert_out=e_host[idx], topk_w=w_host[idx], post_w=pw, pre_w=qw)
+
     outl = synth.bernoulli(cfg.seed, synth.STREAMS["outlier"], T * K, cfg.outlier_p)
     outl_tok = np.unique(np.nonzero(outl)[0] // K)
     rng = np.random.default_rng(4)
     rows = np.unique(np.concatenate([rng.choice(outl_tok, min(512, outl_tok.size), replace=False),
                                      rng.choice(T, 512, replace=False)]))
-    idx = torch.from_numpy(rows).to(DEV)
-    inp = dict(h=h_in[idx].cpu(), expert_out=e[idx].cpu(), topk_w=w[idx].cpu(), post_w=pw,
-               pre_w=qw)
-    want = oracle_moe(inp, cfg.n, cfg.eps)
-    check((bits(h[idx]), bits(y[idx])), want, f"{cfg.name} ({rows.size} sampled rows)")
-    # sampled rows must equal a fresh generation of the same rows (the bytes the oracle saw)
-    r0 = int(rows[0])
-    assert torch.equal(inp["expert_out"][0], synth.expert_rows(cfg, r0, 1)[0])
+    idx = torch.from_numpy(rows)
+    check((h_out[rows], y_out[rows]), oracle_moe(rows_input(idx), cfg.n, cfg.eps),
+          f"{cfg.name} ({rows.size} sampled rows)")
+
+    same_h = same_y = 0
+    for r in range(0, T, 8192):
+        sl = slice(r, min(T, r + 8192))
+        want_h, want_y = oracle_moe(rows_input(sl), cfg.n, cfg.eps)
+        st_h = assert_parity(h_out[sl], want_h, f"{cfg.name} rows {r}.. h'")
+        st_y = assert_parity(y_out[sl], want_y, f"{cfg.name} rows {r}.. y")
+        same_h += st_h["identical"]
+        same_y += st_y["identical"]
+    n = T * D
+    print(f"{cfg.name}: all {T} rows, h' {same_h / n:.6f} and y {same_y / n:.6f} bit-identical")
+    assert same_h == n and same_y == n
 
 
 # --------------------------------------------------------------- shapes and edge cases
@@ -271,19 +286,31 @@ def test_ring_kernel_at_a_hidden_size_where_fewer_slots_fit():
         check(gpu_dense(inp, 3, 1e-6), oracle_dense(inp, 3, 1e-6), f"ring D={D}")
 
 
-def test_bounded_wait_runs_out_reports_timeout_and_leaves_the_context_usable():
-    """The test hook makes every CTA wait on an mbarrier that nothing completes;
-    each wait gives up after 1 ms and the status word reports it."""
-    T, D = 64, 5120
+def test_bounded_wait_runs_out_reports_timeout_and_leaves_later_rows_untouched():
+    """The test hook withholds the bulk copy of each CTA's second row. That slot wait gives
+    up after 1 ms; the CTA stores nothing for that row or any later one (h and y keep
+    their bytes), drains its copies in flight and returns; the status word reports the
+    timeout. Each CTA's first row (rows 0 .. grid-1) is computed exactly. The context
+    stays usable."""
+    T, D = 2048, 5120
     inp = random_dense(T, D, seed=16)
     d = to_dev(inp)
+    sentinel = 0x40E0  # BF16 7.0
+    y = torch.full((T, D), 7.0, dtype=torch.bfloat16, device=DEV)
     opts = dict(flags=snr._lib.BEAM_OPT_TEST_WAIT_TIMEOUT)
-    y = snr.boundary_fused(d["h"], d["x"], d["post_w"], d["pre_w"], 5, 1e-6, opts=opts)
+    snr.boundary_fused(d["h"], d["x"], d["post_w"], d["pre_w"], 5, 1e-6, y=y, opts=opts)
     with pytest.raises(snr.BeamError) as ei:
         snr.sync_status()
     assert ei.value.status == snr._lib.BEAM_ERR_TIMEOUT
-    # the launch carried on: results are still exact
-    check((bits(d["h"]), bits(y)), oracle_dense(inp, 5, 1e-6), "after a timed-out wait")
+    h_out, y_out = bits(d["h"]), bits(y)
+    h_in = oracle.as_u16(inp["h"])
+    written = (y_out != sentinel).any(1)
+    G = int(written.sum())
+    assert 1 <= G < T and written[:G].all(), G  # exactly the first row of every CTA
+    want_h, want_y = oracle_dense(inp, 5, 1e-6)
+    assert np.array_equal(h_out[:G], want_h[:G]) and np.array_equal(y_out[:G], want_y[:G])
+    assert np.array_equal(h_out[G:], h_in[G:]) and (y_out[G:] == sentinel).all()
+    print(f"timed-out launch: {G} first rows computed, {T - G} rows untouched")
     # the status was cleared and the context still works
     snr.sync_status()
     check(gpu_dense(inp, 5, 1e-6), oracle_dense(inp, 5, 1e-6), "next call")
@@ -435,21 +462,16 @@ def _router_inputs(T, seed):
     return z, b
 
 
-def _check_routing(z, b, idx_g, w_g, idx_o, w_o, label):
-    """Exact selections on >= 99.99% of tokens; elsewhere the GPU's choice must be a near-tie
-    of the oracle's (the GPU's FP32 exp may differ by a few ulps). Weights of tokens with the
-    same selection agree to 16 ulps (2^-19 relative)."""
+def _check_routing(idx_g, w_g, idx_o, w_o, label):
+    """Expert ids are index work and the weights are FP32 results of exact steps (the
+    sigmoid is correctly rounded on both sides): both must be identical, bit for bit
+    (NaN weights: NaN on both sides)."""
     same = (idx_g == idx_o).all(1)
-    frac = float(same.mean())
-    s = np.array([[oracle.sigmoid(float(v)) for v in row] for row in z[~same]],
-                 np.float32).reshape(-1, z.shape[1])
-    bb = (s + b).astype(np.float64)
-    for r, (ig, io) in enumerate(zip(idx_g[~same], idx_o[~same])):
-        assert len(set(ig.tolist())) == len(ig)
-        assert np.all(np.abs(bb[r, ig] - bb[r, io]) <= 2.0 ** -19), (label, ig, io)
-    rel = np.abs(w_g[same].astype(np.float64) - w_o[same]) / np.abs(w_o[same])
-    print(f"{label}: identical selections {frac:.6f}, max weight error {rel.max():.3g} rel")
-    assert frac >= 0.9999 and rel.max() <= 2.0 ** -19
+    assert same.all(), (label, np.nonzero(~same)[0][:5], idx_g[~same][:2], idx_o[~same][:2])
+    nan = np.isnan(w_o)
+    assert np.array_equal(np.isnan(w_g), nan), label
+    assert np.array_equal(w_g.view(np.uint32)[~nan], w_o.view(np.uint32)[~nan]), label
+    print(f"{label}: {idx_g.shape[0]} tokens, identical experts and weights")
 
 
 @pytest.mark.parametrize("ng,tg,k,scale", [(8, 4, 8, 2.5), (1, 1, 8, 1.0), (32, 4, 6, 1.0),
@@ -461,26 +483,74 @@ def test_routing_matches_the_oracle(ng, tg, k, scale):
                                scale)
     snr.sync_status()
     idx_o, w_o = oracle.route(z, b, ng, tg, k, scale, threads=THREADS)
-    _check_routing(z, b, idx_g.cpu().numpy(), w_g.cpu().numpy(), idx_o, w_o,
+    _check_routing(idx_g.cpu().numpy(), w_g.cpu().numpy(), idx_o, w_o,
                    f"route ng={ng} tg={tg} k={k}")
 
 
 def test_routing_with_infinite_and_extreme_logits():
-    """Logits of +-inf, +-100 and +-50 beside ordinary ones: the sigmoid saturates
-    to exactly 1 or underflows (the kernel's is 0 below about -88.7, where the
-    correctly rounded value is a subnormal under 3e-39, far below any bias), and the
-    routing stays within the tolerance of the random-logit test."""
+    """Logits of +-inf, +-100, -95 (a subnormal sigmoid) and +-50 beside ordinary ones:
+    the sigmoid saturates to exactly 1, underflows to 0 or is a subnormal, on both sides
+    alike."""
     T = 2048
     z, b = _router_inputs(T, 13)
     rng = np.random.default_rng(13)
-    extremes = np.array([np.inf, -np.inf, 100.0, -100.0, 50.0, -50.0], np.float32)
+    extremes = np.array([np.inf, -np.inf, 100.0, -100.0, -95.0, 50.0, -50.0], np.float32)
     pick = rng.random((T, 256)) < 0.05
     z[pick] = extremes[rng.integers(0, extremes.size, int(pick.sum()))]
     idx_g, w_g = snr.moe_route(torch.from_numpy(z).to(DEV), torch.from_numpy(b).to(DEV))
     snr.sync_status()
     idx_o, w_o = oracle.route(z, b, threads=THREADS)
     assert np.isfinite(w_g.cpu().numpy()).all()
-    _check_routing(z, b, idx_g.cpu().numpy(), w_g.cpu().numpy(), idx_o, w_o, "route extreme logits")
+    _check_routing(idx_g.cpu().numpy(), w_g.cpu().numpy(), idx_o, w_o, "route extreme logits")
+
+
+@pytest.mark.parametrize("ng,tg,k", [(8, 4, 8), (4, 2, 16), (32, 4, 6), (1, 1, 8)])
+def test_routing_with_nan_logits_and_non_finite_bias(ng, tg, k):
+    """NaN logits (2% of them, and whole NaN groups on some tokens), a NaN, a +inf and a
+    -inf correction bias: NaN scores rank below every number on both sides, so the same
+    experts are chosen; weights that involve a NaN score are NaN on both sides."""
+    T = 2048
+    z, b = _router_inputs(T, 14)
+    rng = np.random.default_rng(14)
+    z[rng.random((T, 256)) < 0.02] = np.nan
+    for t in range(16):
+        g = t % 8
+        z[t, 32 * g:32 * g + 32] = np.nan
+    b[7], b[100], b[200] = np.nan, np.inf, -np.inf
+    idx_g, w_g = snr.moe_route(torch.from_numpy(z).to(DEV), torch.from_numpy(b).to(DEV), ng, tg, k,
+                               2.5)
+    snr.sync_status()
+    idx_o, w_o = oracle.route(z, b, ng, tg, k, 2.5, threads=THREADS)
+    _check_routing(idx_g.cpu().numpy(), w_g.cpu().numpy(), idx_o, w_o,
+                   f"route NaN ng={ng} tg={tg} k={k}")
+
+
+@pytest.mark.slow
+def test_router_sigmoid_every_float_matches_the_oracle():
+    """All 2^32 float inputs through the kernel's sigmoid (beam_router_sigmoid, the
+    function the router scores with) against the oracle's correctly rounded sigmoid:
+    identical bits (NaN inputs: NaN outputs)."""
+    chunk = 1 << 28
+    bad = 0
+    for c in range((1 << 32) // chunk):
+        lo = c * chunk
+        start = lo if lo < (1 << 31) else lo - (1 << 32)
+        zg = torch.arange(start, start + chunk, dtype=torch.int32, device=DEV).view(torch.float32)
+        sg = snr.router_sigmoid(zg)
+        snr.sync_status()
+        got = sg.cpu().numpy().view(np.uint32)
+        del zg, sg
+        z = np.arange(lo, lo + chunk, dtype=np.uint32).view(np.float32)
+        want = oracle.sigmoid_array(z, threads=THREADS).view(np.uint32)
+        nan = np.isnan(z)
+        diff = (got != want) & ~nan
+        diff |= nan & ~np.isnan(got.view(np.float32))
+        n = int(diff.sum())
+        if n:
+            print("first differences:", [hex(lo + int(i)) for i in np.nonzero(diff)[0][:5]])
+        bad += n
+    assert bad == 0
+    assert oracle.sigmoid_undecided() == 0
 
 
 @pytest.mark.parametrize("ng,tg,k", [(8, 4, 8), (4, 2, 16), (32, 4, 6)])
@@ -505,10 +575,7 @@ def test_routing_exact_ties_go_to_the_lower_index(ng, tg, k):
                                2.5)
     snr.sync_status()
     idx_o, w_o = oracle.route(z, b, ng, tg, k, 2.5, threads=THREADS)
-    idx_g = idx_g.cpu().numpy()
-    assert np.array_equal(idx_g, idx_o), np.argwhere((idx_g != idx_o).any(1))[:5].ravel()
-    rel = np.abs(w_g.cpu().numpy().astype(np.float64) - w_o) / np.abs(w_o)
-    assert rel.max() <= 2.0 ** -19
+    _check_routing(idx_g.cpu().numpy(), w_g.cpu().numpy(), idx_o, w_o, f"route ties ng={ng}")
 
 
 def test_routing_then_the_scaled_combine_boundary():
