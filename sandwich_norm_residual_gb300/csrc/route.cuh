@@ -115,16 +115,37 @@ __device__ __forceinline__ void pick_rounds_sorted4(uint32_t (&key)[4], uint32_t
     }
 }
 
+// Bound on |b' - b| for a biased score b' = RN32(s' + bias) formed from the
+// fast sigmoid s' instead of the exact s: |s' - s| < 2^-20 (below), plus two
+// ulps of b for the two roundings of the sum, plus the subnormal spacing.
+__device__ __forceinline__ float score_slack(float b) {
+    return __fmaf_rn(fabsf(b), 0x1p-22f, 0x1p-20f + 0x1p-148f);
+}
+
 // NG, TG, K: n_group, topk_group and topk fixed at compile time (0: read from
 // the parameters). Fixed values unroll every loop and turn the group arithmetic
 // into shifts; the arithmetic on the scores is the same either way. When the
 // kept groups hold 128 experts, they are first compacted in shared memory to 4
 // per lane and sorted within the lane, which makes each topk round two warp
 // reductions and a shift.
+//
+// Two passes, the first usually final. Fast pass: every score from the fast
+// FP32 sigmoid s' = RN32(1 / RN32(1 + expf(-z))). CUDA documents expf within
+// 2 ulps, so |s' - s| <= (2^-22 + 2^-23) s < 2^-20, and every biased score,
+// group score and pick then carries a known slack. The choice is accepted when
+// the slack cannot change it: every kept group's score interval lies above
+// every dropped group's, every pick's above every eligible expert left out,
+// and consecutive picks' intervals are disjoint, so the order of the output is
+// fixed too. Then only the picks' exact sigmoids are computed (the weights
+// need them). Exact pass (a logit or bias is NaN, or an interval test failed,
+// for instance on exactly tied scores): every score exact, as defined.
 template <int NG, int TG, int K>
 __global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
     constexpr bool kCompact = NG > 0 && TG > 0 && TG * (kRouteExperts / (NG > 0 ? NG : 1)) == 128;
-    __shared__ __align__(16) float s_all[kRouteWarps][kRouteExperts];  // unbiased scores, per warp
+    __shared__ __align__(16) float zs[kRouteWarps][kRouteExperts];  // logits; unbiased scores in the exact pass
+    __shared__ __align__(16) float bs[kRouteWarps][kRouteExperts];  // fast biased scores
+    __shared__ __align__(16) uint32_t ck[kRouteWarps][128];
+    __shared__ int cb[kRouteWarps][16];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -133,6 +154,8 @@ __global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
     const int n_group = NG ? NG : p.n_group;
     const int topk_group = TG ? TG : p.topk_group;
     const int topk = K ? K : p.topk;
+    const int lpg = 32 / n_group;  // lanes per group (a power of two)
+    const int my_group = lane / lpg;
 
     const float4* z4 = reinterpret_cast<const float4*>(p.logits + t * kRouteExperts + 8 * lane);
     const float4* b4 = reinterpret_cast<const float4*>(p.bias + 8 * lane);
@@ -140,84 +163,150 @@ __global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
     const float z[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
     const float bias[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
     const SigmoidLane lt = sigmoid_lane_table();
-    float s[8];
-    uint32_t bk[8];  // keys of the biased scores
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        s[i] = router_sigmoid(z[i], lt);
-        bk[i] = order_key(__fadd_rn(s[i], bias[i]));
-    }
-    float4* mine4 = reinterpret_cast<float4*>(&s_all[warp][8 * lane]);
-    mine4[0] = make_float4(s[0], s[1], s[2], s[3]);
-    mine4[1] = make_float4(s[4], s[5], s[6], s[7]);
+    float4* zrow = reinterpret_cast<float4*>(&zs[warp][8 * lane]);
+    zrow[0] = za;
+    zrow[1] = zb;
 
-    // ---- group scores: the sum of the two largest biased scores of each group.
-    // Only the two values matter, not which experts hold them, so a running
-    // (largest, second largest) pair of keys suffices.
-    uint32_t m1 = 0u, m2 = 0u;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        m2 = max(m2, min(m1, bk[i]));
-        m1 = max(m1, bk[i]);
-    }
-    const int lpg = 32 / n_group;  // lanes per group (a power of two)
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-        if (off >= lpg) continue;
-        const uint32_t o1 = __shfl_xor_sync(full, m1, off), o2 = __shfl_xor_sync(full, m2, off);
-        m2 = max(min(m1, o1), max(m2, o2));
-        m1 = max(m1, o1);
-    }
-    // every group has at least 8 experts (n_group <= 32), so m1 and m2 are keys
-    // of real scores
-    const uint32_t gkey = order_key(__fadd_rn(key_value(m1), key_value(m2)));
-    const int my_group = lane / lpg;
-
-    // ---- keep the topk_group best groups (one total order: exactly
-    // topk_group groups have a rank below topk_group)
-    int rank = 0;
-#pragma unroll
-    for (int g = 0; g < 32; ++g) {
-        if (g >= n_group) break;
-        const uint32_t kg = __shfl_sync(full, gkey, g * lpg);
-        rank += (kg > gkey || (kg == gkey && g < my_group)) ? 1 : 0;
-    }
-    const bool eligible = rank < topk_group;
-
-    // ---- topk best biased scores among the eligible experts
     int sel_i[kRouteMaxTopk];
     int my_i = 0;
-    if constexpr (kCompact) {
-        // the 16 lanes of kept groups write their biased scores to slots 0..15
-        // in expert order; lane j then holds experts 4j .. 4j+3 of that order
-        __shared__ __align__(16) uint32_t ck[kRouteWarps][128];
-        __shared__ int cb[kRouteWarps][16];
-        const unsigned kept = __ballot_sync(full, eligible);
-        // exactly 16 lanes are kept (4 whole groups of 4 lanes), so slot < 16;
-        // the bound is checked all the same before the shared-memory writes
-        const int slot = __popc(kept & ((1u << (my_group * lpg)) - 1u)) + (lane & (lpg - 1));
-        if (eligible && slot < 16) {
-            uint4* dst = reinterpret_cast<uint4*>(&ck[warp][8 * slot]);
-            dst[0] = make_uint4(bk[0], bk[1], bk[2], bk[3]);
-            dst[1] = make_uint4(bk[4], bk[5], bk[6], bk[7]);
-            cb[warp][slot] = 8 * lane;
-        }
-        __syncwarp();
-        const uint4 v = reinterpret_cast<const uint4*>(ck[warp])[lane];
-        uint32_t key[4] = {v.x, v.y, v.z, v.w};
-        pick_rounds_sorted4(key, (uint32_t)(cb[warp][lane >> 1] + 4 * (lane & 1)), topk, lane, sel_i, my_i);
-    } else {
-        uint32_t key[8];
+    bool eligible = false;
+    uint32_t gkey = 0u, rest = 0u;
+
+    // The choice from the keys of this lane's 8 biased scores: group scores
+    // (sum of the two largest of each group: only the two values matter, so a
+    // running pair of keys suffices), the topk_group best groups on one total
+    // order (exactly topk_group groups rank below topk_group), then the topk
+    // best eligible experts. Leaves in `rest` the key of the best eligible
+    // expert left out (0: none).
+    auto choose = [&](const uint32_t (&bk)[8]) {
+        uint32_t m1 = 0u, m2 = 0u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) key[i] = eligible ? bk[i] : 0u;  // 0: unavailable
-        pick_rounds<8>(key, (uint32_t)(8 * lane), topk, lane, sel_i, my_i);
+        for (int i = 0; i < 8; ++i) {
+            m2 = max(m2, min(m1, bk[i]));
+            m1 = max(m1, bk[i]);
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            if (off >= lpg) continue;
+            const uint32_t o1 = __shfl_xor_sync(full, m1, off), o2 = __shfl_xor_sync(full, m2, off);
+            m2 = max(min(m1, o1), max(m2, o2));
+            m1 = max(m1, o1);
+        }
+        // every group has at least 8 experts (n_group <= 32): m1, m2 are real keys
+        gkey = order_key(__fadd_rn(key_value(m1), key_value(m2)));
+        int rank = 0;
+#pragma unroll
+        for (int g = 0; g < 32; ++g) {
+            if (g >= n_group) break;
+            const uint32_t kg = __shfl_sync(full, gkey, g * lpg);
+            rank += (kg > gkey || (kg == gkey && g < my_group)) ? 1 : 0;
+        }
+        eligible = rank < topk_group;
+        if constexpr (kCompact) {
+            // the 16 lanes of kept groups write their keys to slots 0..15 in
+            // expert order; lane j then holds experts 4j .. 4j+3 of that order.
+            // Exactly 16 lanes are kept (4 whole groups of 4 lanes), so
+            // slot < 16; the bound is checked all the same before the writes.
+            const unsigned kept = __ballot_sync(full, eligible);
+            const int slot = __popc(kept & ((1u << (my_group * lpg)) - 1u)) + (lane & (lpg - 1));
+            if (eligible && slot < 16) {
+                uint4* dst = reinterpret_cast<uint4*>(&ck[warp][8 * slot]);
+                dst[0] = make_uint4(bk[0], bk[1], bk[2], bk[3]);
+                dst[1] = make_uint4(bk[4], bk[5], bk[6], bk[7]);
+                cb[warp][slot] = 8 * lane;
+            }
+            __syncwarp();
+            const uint4 v = reinterpret_cast<const uint4*>(ck[warp])[lane];
+            uint32_t key[4] = {v.x, v.y, v.z, v.w};
+            pick_rounds_sorted4(key, (uint32_t)(cb[warp][lane >> 1] + 4 * (lane & 1)), topk, lane, sel_i, my_i);
+            rest = __reduce_max_sync(full, key[0]);  // lists stay sorted: the first is the best left
+            __syncwarp();                            // ck and cb are reused by a later call
+        } else {
+            uint32_t key[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) key[i] = eligible ? bk[i] : 0u;  // 0: unavailable
+            pick_rounds<8>(key, (uint32_t)(8 * lane), topk, lane, sel_i, my_i);
+            uint32_t mk = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mk = max(mk, key[i]);
+            rest = __reduce_max_sync(full, mk);
+        }
+    };
+
+    // ---- fast pass
+    bool finite_in = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) finite_in &= (z[i] == z[i]) && (bias[i] == bias[i]);
+    if (__all_sync(full, finite_in)) {
+        uint32_t bk[8];
+        float bv[8], amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float sf = __frcp_rn(__fadd_rn(1.0f, expf(-z[i])));
+            bv[i] = __fadd_rn(sf, bias[i]);
+            bk[i] = order_key(bv[i]);
+            amax = fmaxf(amax, fabsf(bv[i]));
+        }
+        float4* brow = reinterpret_cast<float4*>(&bs[warp][8 * lane]);
+        brow[0] = make_float4(bv[0], bv[1], bv[2], bv[3]);
+        brow[1] = make_float4(bv[4], bv[5], bv[6], bv[7]);
+        choose(bk);
+        // groups: the kept ones' score intervals above the dropped ones'
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            if (off >= lpg) continue;
+            amax = fmaxf(amax, __shfl_xor_sync(full, amax, off));
+        }
+        const float g = key_value(gkey);
+        const float dg = __fadd_rn(__fmul_rn(2.0f, score_slack(amax)), score_slack(g));
+        const float glo = eligible ? __fsub_rn(g, dg) : INFINITY;
+        const float ghi = eligible ? -INFINITY : __fadd_rn(g, dg);
+        // picks: each pick's interval above the next pick's and above the best
+        // eligible expert left out
+        __syncwarp();
+        const float bsel = lane < topk ? bs[warp][my_i] : 0.0f;
+        const float bnext = __shfl_down_sync(full, bsel, 1);
+        const float slo = lane < topk ? __fsub_rn(bsel, score_slack(bsel)) : INFINITY;
+        const float rv = key_value(rest);
+        const float rhi = rest ? __fadd_rn(rv, score_slack(rv)) : -INFINITY;
+        bool ok = glo == glo && ghi == ghi && slo == slo && rhi == rhi;
+        ok &= (lane + 1 >= topk) || slo > __fadd_rn(bnext, score_slack(bnext));
+        const float glo_min = key_value(__reduce_min_sync(full, order_key(glo)));
+        const float ghi_max = key_value(__reduce_max_sync(full, order_key(ghi)));
+        const float slo_min = key_value(__reduce_min_sync(full, order_key(slo)));
+        ok &= glo_min > ghi_max && slo_min > rhi;
+        if (__all_sync(full, ok)) {
+            // the choice is the exact one: the picks' exact sigmoids give the weights
+            const float sk = router_sigmoid(lane < topk ? zs[warp][my_i] : 0.0f, lt);
+            float sum = __shfl_sync(full, sk, 0);
+#pragma unroll
+            for (int k = 1; k < kRouteMaxTopk; ++k)
+                if (k < topk) sum = __fadd_rn(sum, __shfl_sync(full, sk, k));
+            if (lane < topk) {
+                p.idx[t * topk + lane] = my_i;
+                p.w[t * topk + lane] = __fmul_rn(__fdiv_rn(sk, sum), p.scale);
+            }
+            return;
+        }
     }
 
-    // ---- weights: unbiased scores of the picks, renormalised in output order
-    // (the sum reads the same address in every lane), scaled; lane k < topk
-    // writes output k (one division per lane)
+    // ---- exact pass: every score exact
+    float sv[8];
+    uint32_t bk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        sv[i] = router_sigmoid(z[i], lt);
+        bk[i] = order_key(__fadd_rn(sv[i], bias[i]));
+    }
     __syncwarp();
-    const float* sw = s_all[warp];
+    zrow[0] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+    zrow[1] = make_float4(sv[4], sv[5], sv[6], sv[7]);
+    choose(bk);
+    // weights: unbiased scores of the picks, renormalised in output order (the
+    // sum reads the same address in every lane), scaled; lane k < topk writes
+    // output k (one division per lane)
+    __syncwarp();
+    const float* sw = zs[warp];
     float sum = sw[sel_i[0]];
 #pragma unroll
     for (int k = 1; k < kRouteMaxTopk; ++k)

@@ -15,6 +15,30 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
 
+// L2 cache policies: evict_last keeps lines ahead of normal and evict_first
+// ones; evict_first lines are the first to go. A later access with another
+// policy sets the line's priority anew.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// The same prefetch, with the lines marked evict_last so that the write
+// stream of the rows being finished does not push them out before they are
+// read. Every caller reads the prefetched lines with an evict_first load (or
+// overwrites them with evict_first stores), which drops the priority again:
+// no evict_last line outlives the kernel.
+__device__ __forceinline__ void prefetch_l2_keep(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;"
+                 :: "l"(p), "r"(bytes), "l"(l2_evict_last()) : "memory");
+}
+
 // Programmatic dependent launch. A kernel launched with programmatic stream
 // serialisation may start while the previous kernel on the stream still runs;
 // pdl_wait() returns once that kernel has completed and its writes are
