@@ -59,7 +59,7 @@ constexpr int kTopK = 8;
 // and that these loads then consume (measured on GB300 at T = 16384: the MoE
 // boundary 281 -> 272 us, the dense boundary 114.5 -> 113.5 us).
 
-// read-only operands (x, expert rows)
+// read-only operands (expert rows; never h)
 __device__ __forceinline__ uint4 ld_stream_ro(const void* p) {
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
@@ -67,7 +67,8 @@ __device__ __forceinline__ uint4 ld_stream_ro(const void* p) {
     return r;
 }
 
-// h is read here and overwritten later by the same thread: no .nc
+// h (read here and overwritten later by the same thread) and x (which may be
+// h itself): no .nc
 __device__ __forceinline__ uint4 ld_stream_rw(const void* p) {
     uint4 r;
     asm("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
@@ -462,7 +463,9 @@ __global__ void __launch_bounds__(kMaxThreads) boundary_kernel(const BoundaryPar
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int vi = tid + i * nt;
-                xv[i] = (FULL || vi < p.nvec) ? ld_stream_ro(p.x + base + (size_t)vi * 8) : make_uint4(0, 0, 0, 0);
+                // x may be h itself, which this kernel writes: x takes the
+                // coherent load, not the read-only path (measured the same speed)
+                xv[i] = (FULL || vi < p.nvec) ? ld_stream_rw(p.x + base + (size_t)vi * 8) : make_uint4(0, 0, 0, 0);
             }
         }
 #pragma unroll
