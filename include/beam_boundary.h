@@ -188,6 +188,15 @@ BEAM_API beam_status beam_moe_route(beam_stream_t stream, const float* logits, c
  */
 BEAM_API beam_status beam_router_sigmoid(beam_stream_t stream, const float* z, float* s, int64_t count);
 
+/*
+ * The fast FP32 sigmoid of beam_moe_route's first pass, elementwise (the
+ * pass that chooses the experts when interval tests show the choice cannot
+ * change; see beam_moe_route). Not correctly rounded: s[i] lies within 2^-19
+ * of the exact sigmoid for every float input, NaN gives NaN. Exposed so that
+ * this bound can be checked; arguments and errors as beam_router_sigmoid.
+ */
+BEAM_API beam_status beam_router_sigmoid_fast(beam_stream_t stream, const float* z, float* s, int64_t count);
+
 /* Head dimension and modes of beam_qk_norm. */
 #define BEAM_QK_HEAD_DIM 128
 #define BEAM_QK_ROPE 0

@@ -323,9 +323,10 @@ def moe_route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8
     return idx, w
 
 
-def router_sigmoid(z, out=None, stream=None):
+def router_sigmoid(z, out=None, stream=None, fast: bool = False):
     """The router's correctly rounded FP32 sigmoid of every element of ``z`` (float32 CUDA
-    tensor, any shape, contiguous); ``out`` may be ``z`` (in place)."""
+    tensor, any shape, contiguous); ``out`` may be ``z`` (in place). With ``fast``, the
+    routing first pass's approximation instead (within 2^-19 of the exact sigmoid)."""
     import torch
     if not isinstance(z, torch.Tensor) or z.dtype != torch.float32 or not z.is_contiguous():
         raise TypeError("z must be a contiguous float32 tensor")
@@ -335,9 +336,10 @@ def router_sigmoid(z, out=None, stream=None):
         raise TypeError("out must be a contiguous float32 tensor")
     _shape(out, "out", tuple(z.shape))
     _on_current_device(z=z, out=out)
-    st = _lib.load().beam_router_sigmoid(_stream_ptr(stream), z.data_ptr(), out.data_ptr(), z.numel())
+    fn = _lib.load().beam_router_sigmoid_fast if fast else _lib.load().beam_router_sigmoid
+    st = fn(_stream_ptr(stream), z.data_ptr(), out.data_ptr(), z.numel())
     if st != 0:
-        raise BeamError(st, "beam_router_sigmoid")
+        raise BeamError(st, "beam_router_sigmoid_fast" if fast else "beam_router_sigmoid")
     return out
 
 

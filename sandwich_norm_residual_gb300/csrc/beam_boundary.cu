@@ -622,7 +622,7 @@ beam_status beam_moe_route(beam_stream_t stream, const float* logits, const floa
     return BEAM_OK;
 }
 
-beam_status beam_router_sigmoid(beam_stream_t stream, const float* z, float* s, int64_t count) {
+static beam_status router_sigmoid_call(beam_stream_t stream, const float* z, float* s, int64_t count, int fast) {
     if (count < 0 || count > (int64_t(1) << 40)) return BEAM_ERR_SHAPE;
     if (count == 0) return BEAM_OK;
     if (!z || !s) return BEAM_ERR_NULL;
@@ -635,9 +635,18 @@ beam_status beam_router_sigmoid(beam_stream_t stream, const float* z, float* s, 
     int64_t blocks = (count + 255) / 256;
     const int64_t cap = (int64_t)info->sms * 8;  // grid-stride beyond 8 blocks per SM
     if (blocks > cap) blocks = cap;
-    beam::router_sigmoid_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(z, s, count);
+    beam::router_sigmoid_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(z, s, count,
+                                                                                                    fast);
     if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
     return BEAM_OK;
+}
+
+beam_status beam_router_sigmoid(beam_stream_t stream, const float* z, float* s, int64_t count) {
+    return router_sigmoid_call(stream, z, s, count, 0);
+}
+
+beam_status beam_router_sigmoid_fast(beam_stream_t stream, const float* z, float* s, int64_t count) {
+    return router_sigmoid_call(stream, z, s, count, 1);
 }
 
 beam_status beam_moe_combine_boundary(beam_stream_t stream, uint16_t* h, const uint16_t* expert_out,

@@ -116,10 +116,10 @@ __device__ __forceinline__ void pick_rounds_sorted4(uint32_t (&key)[4], uint32_t
 }
 
 // Bound on |b' - b| for a biased score b' = RN32(s' + bias) formed from the
-// fast sigmoid s' instead of the exact s: |s' - s| < 2^-20 (below), plus two
-// ulps of b for the two roundings of the sum, plus the subnormal spacing.
+// fast sigmoid s' instead of the exact s: |s' - s| < kFastSigmoidSlack, plus
+// two ulps of b for the two roundings of the sum, plus the subnormal spacing.
 __device__ __forceinline__ float score_slack(float b) {
-    return __fmaf_rn(fabsf(b), 0x1p-22f, 0x1p-20f + 0x1p-148f);
+    return __fmaf_rn(fabsf(b), 0x1p-22f, kFastSigmoidSlack + 0x1p-148f);
 }
 
 // NG, TG, K: n_group, topk_group and topk fixed at compile time (0: read from
@@ -130,9 +130,9 @@ __device__ __forceinline__ float score_slack(float b) {
 // reductions and a shift.
 //
 // Two passes, the first usually final. Fast pass: every score from the fast
-// FP32 sigmoid s' = RN32(1 / RN32(1 + expf(-z))). CUDA documents expf within
-// 2 ulps, so |s' - s| <= (2^-22 + 2^-23) s < 2^-20, and every biased score,
-// group score and pick then carries a known slack. The choice is accepted when
+// FP32 sigmoid s' (router_sigmoid_fast, within 2^-19 of the exact sigmoid on
+// every float input), so every biased score, group score and pick carries a
+// known slack. The choice is accepted when
 // the slack cannot change it: every kept group's score interval lies above
 // every dropped group's, every pick's above every eligible expert left out,
 // and consecutive picks' intervals are disjoint, so the order of the output is
@@ -175,9 +175,8 @@ __global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
     // The choice from the keys of this lane's 8 biased scores: group scores
     // (sum of the two largest of each group: only the two values matter, so a
     // running pair of keys suffices), the topk_group best groups on one total
-    // order (exactly topk_group groups rank below topk_group), then the topk
-    // best eligible experts. Leaves in `rest` the key of the best eligible
-    // expert left out (0: none).
+    // order (ties to the lower group), then the topk best eligible experts.
+    // Leaves in `rest` the key of the best eligible expert left out (0: none).
     auto choose = [&](const uint32_t (&bk)[8]) {
         uint32_t m1 = 0u, m2 = 0u;
 #pragma unroll
@@ -194,14 +193,17 @@ __global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
         }
         // every group has at least 8 experts (n_group <= 32): m1, m2 are real keys
         gkey = order_key(__fadd_rn(key_value(m1), key_value(m2)));
-        int rank = 0;
+        // topk_group rounds of two warp reductions: the largest key among the
+        // groups not yet kept, then the lowest group index holding it (every
+        // lane of a group holds its group's key; keys are never 0)
+        eligible = false;
 #pragma unroll
-        for (int g = 0; g < 32; ++g) {
-            if (g >= n_group) break;
-            const uint32_t kg = __shfl_sync(full, gkey, g * lpg);
-            rank += (kg > gkey || (kg == gkey && g < my_group)) ? 1 : 0;
+        for (int r = 0; r < 32; ++r) {
+            if (r >= topk_group) break;
+            const uint32_t m = __reduce_max_sync(full, eligible ? 0u : gkey);
+            const uint32_t gw = __reduce_min_sync(full, (!eligible && gkey == m) ? (uint32_t)my_group : 0xFFFFFFFFu);
+            eligible |= (uint32_t)my_group == gw;
         }
-        eligible = rank < topk_group;
         if constexpr (kCompact) {
             // the 16 lanes of kept groups write their keys to slots 0..15 in
             // expert order; lane j then holds experts 4j .. 4j+3 of that order.
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
         float bv[8], amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float sf = __frcp_rn(__fadd_rn(1.0f, expf(-z[i])));
+            const float sf = router_sigmoid_fast(z[i]);
             bv[i] = __fadd_rn(sf, bias[i]);
             bk[i] = order_key(bv[i]);
             amax = fmaxf(amax, fabsf(bv[i]));
@@ -317,15 +319,16 @@ __global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
     }
 }
 
-// The router's sigmoid alone, elementwise: s[i] = RN32(1 / (1 + e^-z[i])).
-// Whole warps iterate together (the sigmoid reads its table by shuffle).
-__global__ void __launch_bounds__(256) router_sigmoid_kernel(const float* z, float* s, long long n) {
+// The router's sigmoid alone, elementwise: s[i] = RN32(1 / (1 + e^-z[i])),
+// or (fast) the first pass's approximation. Whole warps iterate together (the
+// exact sigmoid reads its table by shuffle).
+__global__ void __launch_bounds__(256) router_sigmoid_kernel(const float* z, float* s, long long n, int fast) {
     const SigmoidLane lt = sigmoid_lane_table();
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < n; base += stride) {
         const long long i = base + (threadIdx.x & 31);
         const float zi = i < n ? z[i] : 0.0f;
-        const float si = router_sigmoid(zi, lt);
+        const float si = fast ? router_sigmoid_fast(zi) : router_sigmoid(zi, lt);
         if (i < n) s[i] = si;
     }
 }

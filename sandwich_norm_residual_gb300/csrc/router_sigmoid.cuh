@@ -313,6 +313,20 @@ __device__ __forceinline__ float router_sigmoid_ff(float z, SigmoidLane lt, bool
     return res;
 }
 
+// A fast FP32 sigmoid for the router's first pass, 1 / (1 + 2^(-z log2 e))
+// from the hardware's approximate base-2 exponential and reciprocal (ftz).
+// Not correctly rounded: its distance to the exact sigmoid stays below
+// kFastSigmoidSlack on every float input (NaN gives NaN), which a test checks
+// on all 2^32 of them against the correctly rounded oracle.
+constexpr float kFastSigmoidSlack = 0x1p-19f;
+
+__device__ __forceinline__ float router_sigmoid_fast(float z) {
+    float e, s;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(__fmul_rn(z, -1.44269504088896340736f)));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(s) : "f"(__fadd_rn(1.0f, e)));
+    return s;
+}
+
 // The correctly rounded sigmoid. Call with all 32 lanes of the warp (phase 1
 // reads the table by shuffle); phase 2 runs only in the lanes that need it.
 __device__ __forceinline__ float router_sigmoid(float z, SigmoidLane lt) {
