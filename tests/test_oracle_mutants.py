@@ -63,8 +63,7 @@ MUTANTS = [
     ("routing chooses by the unbiased score", "            b[e] = s[e] + bias[e];", "            b[e] = s[e];"),
     ("routing weights from the biased score", "        for (int k = 0; k < topk; ++k) {\n            float q = s[id[k]] / sum;",
      "        for (int k = 0; k < topk; ++k) {\n            float q = b[id[k]] / sum;"),
-    ("routing ties to the higher index", "        if (best < 0 || v[i] > v[best]) best = i;",
-     "        if (best < 0 || v[i] >= v[best]) best = i;"),
+    ("routing ties to the higher index", "    return isnan(b) || a > b;", "    return isnan(b) || a >= b;"),
     ("routing weights not renormalised", "            float q = s[id[k]] / sum;", "            float q = s[id[k]];"),
     ("routing scale not applied", "            w_out[t * topk + k] = q * scale;", "            w_out[t * topk + k] = q;"),
     ("routing sigmoid of the wrong sign", "hi = z >= 0.0f ? 1.0 / (1.0 + e) : e / (1.0 + e);",
