@@ -38,14 +38,14 @@ WORKLOAD = (f"layer boundary pair, T={T_TOKENS} tokens per GPU, D={D}: dense bou
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "moe": {"bytes_per_launch": 1_517_554_000 + 292_852_480, "source_sha": "eace306d18f982cc"},
-    "dense": {"bytes_per_launch": 335_710_000 + 275_014_912, "source_sha": "eace306d18f982cc"},
+    "moe": {"bytes_per_launch": 1_511_117_056 + 300_662_016, "source_sha": "0829ef0db95c6fc6"},
+    "dense": {"bytes_per_launch": 335_659_520 + 264_510_464, "source_sha": "0829ef0db95c6fc6"},
 }
 
 # Routing is bound by instruction issue, not HBM: its warp-instructions per
 # launch at T = 16384 (ncu smsp__inst_executed.sum) give its issue roofline,
 # valid while the kernel source matches.
-ROUTE_ISSUE = {"warp_instructions_per_launch": 8_699_904, "source_sha": "eace306d18f982cc"}
+ROUTE_ISSUE = {"warp_instructions_per_launch": 11_191_944, "source_sha": "0829ef0db95c6fc6"}
 
 
 def kernel_source_sha() -> str:
