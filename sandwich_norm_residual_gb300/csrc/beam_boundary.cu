@@ -695,10 +695,9 @@ beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k, cons
     p.nk = n_kv_heads;
     p.eps = eps;
     p.errk = error_factor_terms(8.0, 2 + 2);  // 8 terms per FP32 lane, 2 merges in the lane + 2 shuffle levels
-    p.mode = mode;
     p.flags = (flags & BEAM_OPT_FORCE_EXACT_SUM) ? beam::kFlagForceExact : 0u;
-    // one warp per token when there are enough tokens to fill the GPU (about 24
-    // warps per SM); with fewer, up to one warp per 8-head batch of a token
+    // one warp per token when there are enough tokens to fill the GPU (16 to 24
+    // resident warps per SM); with fewer, up to one warp per 8-head batch of a token
     const int nbat = (n_q_heads + n_kv_heads + beam::kQKBatch - 1) / beam::kQKBatch;
     const int64_t target = (int64_t)info->sms * 24;
     int wpt = 1;
@@ -710,6 +709,9 @@ beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k, cons
     p.warps_per_token = (nbat + p.batches_per_warp - 1) / p.batches_per_warp;
     const int64_t blocks = (T * p.warps_per_token + 7) / 8;  // 8 warps per block
     if (blocks > 0x7FFFFFFF) return BEAM_ERR_SHAPE;
+    const void* fn = mode == BEAM_QK_ROPE ? reinterpret_cast<const void*>(beam::qk_norm_kernel<0>)
+                                          : reinterpret_cast<const void*>(beam::qk_norm_kernel<1>);
+    void* args[] = {&p};
     if (flags & BEAM_OPT_PDL) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -720,15 +722,17 @@ beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k, cons
         cfg.stream = reinterpret_cast<cudaStream_t>(stream);
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        void* args[] = {&p};
-        if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(beam::qk_norm_kernel), args) != cudaSuccess) {
+        if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
             cudaGetLastError();
             return BEAM_ERR_CUDA;
         }
         return BEAM_OK;
     }
-    beam::qk_norm_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+    if (cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(256), args, 0, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return BEAM_ERR_CUDA;
+    }
     return BEAM_OK;
 }
 
