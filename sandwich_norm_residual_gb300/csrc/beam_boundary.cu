@@ -696,10 +696,10 @@ beam_status beam_qk_norm_ex(beam_stream_t stream, uint16_t* q, uint16_t* k, cons
     p.eps = eps;
     p.errk = error_factor_terms(8.0, 2 + 2);  // 8 terms per FP32 lane, 2 merges in the lane + 2 shuffle levels
     p.flags = (flags & BEAM_OPT_FORCE_EXACT_SUM) ? beam::kFlagForceExact : 0u;
-    // one warp per token when there are enough tokens to fill the GPU (16 to 24
+    // one warp per token when there are enough tokens to fill the GPU (16
     // resident warps per SM); with fewer, up to one warp per 8-head batch of a token
     const int nbat = (n_q_heads + n_kv_heads + beam::kQKBatch - 1) / beam::kQKBatch;
-    const int64_t target = (int64_t)info->sms * 24;
+    const int64_t target = (int64_t)info->sms * 16;
     int wpt = 1;
     if (T < target) {
         const int64_t want = (target + T - 1) / T;

@@ -14,8 +14,8 @@
 // One warp per token walks its heads, 8 heads per pass (4 lanes each), after
 // asking L2 for all of the token's rows. Lane i of a head's group holds elements 16i .. 16i+15
 // and 64+16i .. 64+16i+15: both halves of every rotate-half pair are in the
-// same lane, which keeps its 16 cos and 16 sin values in registers for the
-// whole token. Each lane folds its 32 squares into two compensated sums; the
+// same lane, which reads its 16 cos and 16 sin values from the token's table
+// row, staged once per warp in shared memory. Each lane folds its 32 squares into two compensated sums; the
 // row sum merges them in the lane, then over 2 shuffle levels (4 merge levels
 // in all). Against 8 lanes per head, 4 lanes halve the per-head work that
 // every lane of a group repeats (merges, certification, 1/sqrt): measured
@@ -124,13 +124,14 @@ __device__ __noinline__ float exact_group_sum_squares(uint4 a, uint4 b, uint4 c,
 
 // MODE 0: RoPE, 1: SSMax. Each warp keeps two batches in registers: the next
 // batch is loaded before the current one is processed, while the token's rows
-// are already on their way to L2. The registers this takes set the residency:
-// RoPE, which also holds its 16 cos and 16 sin values, runs 2 blocks of 8 warps
-// per SM (at most 128 registers), SSMax 3 (at most 80). Measured against one
-// batch in flight at 3 blocks per SM for both modes: RoPE 112.9 -> 109.0 us,
-// SSMax 96.1 -> 85.5 us at T = 16384 (three batches in flight were slower).
+// are already on their way to L2; 2 blocks of 8 warps per SM (at most 128
+// registers). Measured at T = 16384 against one batch in flight at 3 blocks per
+// SM: RoPE 112.9 -> 109.0 us, SSMax 96.1 -> 85.5 us at 3 blocks and 83.9 us at
+// 2 (three batches in flight were slower); RoPE's cos and sin read per batch
+// from shared memory instead of held in 32 registers for the whole token:
+// 109.2 -> 101.2 us.
 template <int MODE>
-__global__ void __launch_bounds__(256, MODE == 0 ? 2 : 3) qk_norm_kernel(const QKParams p) {
+__global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
     const int lane = threadIdx.x & 31, grp = lane >> 2, li = lane & 3;
     // warp gw takes heads [hbeg, hend) of token gw / warps_per_token
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -181,17 +182,13 @@ __global__ void __launch_bounds__(256, MODE == 0 ? 2 : 3) qk_norm_kernel(const Q
     uint4 v[4];
     load(v, hbeg);
 
-    float2 cv[8], sv[8];
+    // RoPE: the token's table row (64 cos, then 64 sin), one row per warp
+    __shared__ __align__(16) float tab[8][kQKHeadDim];
+    const float4* cs = reinterpret_cast<const float4*>(&tab[threadIdx.x >> 5][16 * li]);
     if (MODE == 0) {
-        const float4* cs = reinterpret_cast<const float4*>(p.table + pos * kQKHeadDim + 16 * li);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float4 c = __ldg(cs + i), sn = __ldg(cs + 16 + i);
-            cv[2 * i] = make_float2(c.x, c.y);
-            cv[2 * i + 1] = make_float2(c.z, c.w);
-            sv[2 * i] = make_float2(sn.x, sn.y);
-            sv[2 * i + 1] = make_float2(sn.z, sn.w);
-        }
+        reinterpret_cast<float4*>(&tab[threadIdx.x >> 5][0])[lane] =
+            __ldg(reinterpret_cast<const float4*>(p.table + pos * kQKHeadDim) + lane);
+        __syncwarp();
     }
     const float g = MODE != 0 ? ssmax_scale(pos, lane) : 1.0f;
 
@@ -237,6 +234,15 @@ __global__ void __launch_bounds__(256, MODE == 0 ? 2 : 3) qk_norm_kernel(const Q
 #pragma unroll
         for (int i = 0; i < 16; ++i) n[i] = f2_to_bf2(mul2_rn(mul2_rn(bf2_to_f2(w[i]), rv), bf2_to_f2(ww[i])));
         if (MODE == 0) {
+            float2 cv[8], sv[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 c = cs[i], sn = cs[16 + i];
+                cv[2 * i] = make_float2(c.x, c.y);
+                cv[2 * i + 1] = make_float2(c.z, c.w);
+                sv[2 * i] = make_float2(sn.x, sn.y);
+                sv[2 * i + 1] = make_float2(sn.z, sn.w);
+            }
             // words i (elements j) and i + 8 (elements j + 64) form the pairs.
             // The products are packed; the sums are scalar __fadd_rn /
             // __fsub_rn, which never merge into an FMA (a packed add whose only
