@@ -38,14 +38,14 @@ WORKLOAD = (f"layer boundary pair, T={T_TOKENS} tokens per GPU, D={D}: dense bou
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "moe": {"bytes_per_launch": 1_511_117_056 + 300_662_016, "source_sha": "0829ef0db95c6fc6"},
-    "dense": {"bytes_per_launch": 335_659_520 + 264_510_464, "source_sha": "0829ef0db95c6fc6"},
+    "moe": {"bytes_per_launch": 1_511_332_096 + 301_274_880, "source_sha": "0f806eb8112c1325"},
+    "dense": {"bytes_per_launch": 335_650_560 + 264_166_912, "source_sha": "0f806eb8112c1325"},
 }
 
 # Routing is bound by instruction issue, not HBM: its warp-instructions per
 # launch at T = 16384 (ncu smsp__inst_executed.sum) give its issue roofline,
 # valid while the kernel source matches.
-ROUTE_ISSUE = {"warp_instructions_per_launch": 11_191_944, "source_sha": "0829ef0db95c6fc6"}
+ROUTE_ISSUE = {"warp_instructions_per_launch": 11_191_944, "source_sha": "0f806eb8112c1325"}
 
 
 def kernel_source_sha() -> str:
