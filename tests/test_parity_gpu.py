@@ -632,7 +632,11 @@ def _qk_case(T, nq, nk, seed, max_pos):
 
 
 @pytest.mark.parametrize("mode", ["rope", "ssmax"])
-@pytest.mark.parametrize("T,nq,nk", [(16384, 48, 8), (5, 3, 1), (33, 48, 8), (7, 0, 8), (2, 48, 0)])
+# T = 16384: one warp walks all 7 batches of its token; T = 700 and 1000: a
+# token's batches split over several warps of 2 or 3 batches each (ragged last
+# batch at 45 + 7 heads), which runs the two-batch pipeline on short runs
+@pytest.mark.parametrize("T,nq,nk", [(16384, 48, 8), (5, 3, 1), (33, 48, 8), (7, 0, 8), (2, 48, 0),
+                                     (700, 48, 8), (1000, 45, 7)])
 def test_qk_norm_matches_the_oracle(mode, T, nq, nk):
     max_pos = 4096 if mode == "rope" else 1 << 20
     q, k, qw, kw, pos, table = _qk_case(T, nq, nk, T + nq, max_pos if mode == "rope" else 64)
