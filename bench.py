@@ -351,10 +351,11 @@ def decode_latency(snr, device, replays: int = 20) -> dict:
     i64 = torch.empty((64, 8), dtype=torch.int32, device=device)
     w64 = torch.empty((64, 8), dtype=torch.float32, device=device)
 
-    def body4():
-        for _ in range(52):
-            snr.moe_route(z64, b64, idx=i64, w=w64, stream=stream)
-    out["route_T64_us_per_layer"] = timed_graph(body4, "route", replays) / 52
+    for pdl in (False, True):
+        def body4(pdl=pdl):
+            for _ in range(52):
+                snr.moe_route(z64, b64, idx=i64, w=w64, stream=stream, pdl=pdl)
+        out[f"route_T64_us_per_layer{'_pdl' if pdl else ''}"] = timed_graph(body4, "route", replays) / 52
     # the dense chain launched one call at a time, no graph
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):

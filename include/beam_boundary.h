@@ -175,6 +175,17 @@ BEAM_API beam_status beam_moe_route(beam_stream_t stream, const float* logits, c
                                     float route_scale, int32_t* topk_idx, float* topk_w);
 
 /*
+ * beam_moe_route with BEAM_OPT_* flags: BEAM_OPT_PDL launches the kernel with
+ * programmatic stream serialisation, so that it may start while the previous
+ * kernel on the stream finishes; it reads its inputs only after that kernel
+ * has completed. Any other flag gives BEAM_ERR_ARG.
+ */
+BEAM_API beam_status beam_moe_route_ex(beam_stream_t stream, const float* logits, const float* bias,
+                                       int64_t T, int E, int n_group, int topk_group, int topk,
+                                       float route_scale, int32_t* topk_idx, float* topk_w,
+                                       uint32_t flags);
+
+/*
  * The router's FP32 sigmoid alone, elementwise (vLLM page, "MoE and residual
  * stream": expert scores are the sigmoid of the router logits; SGLang page,
  * "Dense layers and grouped MoE routing": FP32 routing). s[i] is the float

@@ -294,10 +294,11 @@ def moe_combine_boundary_nvfp4(h, expert_out, topk_w, post_w, pre_w, n: int, eps
 
 
 def moe_route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8,
-              route_scale: float = 2.5, idx=None, w=None, stream=None):
+              route_scale: float = 2.5, idx=None, w=None, stream=None, pdl: bool = False):
     """Group-limited top-k routing on torch CUDA tensors.
 
     logits: [T, 256] float32 router logits; bias: [256] float32 correction bias.
+    pdl: launch with programmatic dependent launch (BEAM_OPT_PDL).
     Returns (idx int32 [T, topk], w float32 [T, topk]).
     """
     import torch
@@ -315,11 +316,11 @@ def moe_route(logits, bias, n_group: int = 8, topk_group: int = 4, topk: int = 8
     _shape(idx, "idx", (T, topk))
     _shape(w, "w", (T, topk))
     _on_current_device(logits=logits, bias=bias, idx=idx, w=w)
-    st = _lib.load().beam_moe_route(_stream_ptr(stream), logits.data_ptr(), bias.data_ptr(), T, E,
-                                    int(n_group), int(topk_group), int(topk), float(route_scale),
-                                    idx.data_ptr(), w.data_ptr())
+    st = _lib.load().beam_moe_route_ex(_stream_ptr(stream), logits.data_ptr(), bias.data_ptr(), T, E,
+                                       int(n_group), int(topk_group), int(topk), float(route_scale),
+                                       idx.data_ptr(), w.data_ptr(), _lib.BEAM_OPT_PDL if pdl else 0)
     if st != 0:
-        raise BeamError(st, "beam_moe_route")
+        raise BeamError(st, "beam_moe_route_ex")
     return idx, w
 
 

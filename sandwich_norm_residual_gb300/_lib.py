@@ -56,6 +56,7 @@ SIGNATURES = {
     "beam_moe_combine_boundary_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _i64, _i32,
                                                _vp]),
     "beam_moe_route": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
+    "beam_moe_route_ex": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _u32]),
     "beam_router_sigmoid": (_i32, [_vp, _vp, _vp, _i64]),
     "beam_router_sigmoid_fast": (_i32, [_vp, _vp, _vp, _i64]),
     "beam_qk_norm": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _f32,

@@ -582,12 +582,13 @@ beam_status beam_moe_combine_boundary_scaled(beam_stream_t stream, uint16_t* h, 
                         nullptr);
 }
 
-beam_status beam_moe_route(beam_stream_t stream, const float* logits, const float* bias, int64_t T, int E,
-                           int n_group, int topk_group, int topk, float route_scale, int32_t* topk_idx,
-                           float* topk_w) {
+beam_status beam_moe_route_ex(beam_stream_t stream, const float* logits, const float* bias, int64_t T, int E,
+                              int n_group, int topk_group, int topk, float route_scale, int32_t* topk_idx,
+                              float* topk_w, uint32_t flags) {
     if (T < 0 || T > (int64_t(1) << 40) || E != BEAM_ROUTE_EXPERTS) return BEAM_ERR_SHAPE;
     if (n_group < 1 || n_group > 32 || (n_group & (n_group - 1)) || topk_group < 1 || topk_group > n_group ||
-        topk < 1 || topk > BEAM_ROUTE_MAX_TOPK || topk > topk_group * (E / n_group) || !std::isfinite(route_scale))
+        topk < 1 || topk > BEAM_ROUTE_MAX_TOPK || topk > topk_group * (E / n_group) || !std::isfinite(route_scale) ||
+        (flags & ~BEAM_OPT_PDL))
         return BEAM_ERR_ARG;
     if (T == 0) return BEAM_OK;
     if (!logits || !bias || !topk_idx || !topk_w) return BEAM_ERR_NULL;
@@ -614,12 +615,37 @@ beam_status beam_moe_route(beam_stream_t stream, const float* logits, const floa
     const int64_t blocks = (T + beam::kRouteWarps - 1) / beam::kRouteWarps;  // one token per warp
     if (blocks > 0x7FFFFFFF) return BEAM_ERR_SHAPE;
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if (n_group == 8 && topk_group == 4 && topk == 8)  // the Beam / DeepSeek-V3 router
-        beam::route_kernel<8, 4, 8><<<(unsigned)blocks, 256, 0, cs>>>(p);
-    else
-        beam::route_kernel<0, 0, 0><<<(unsigned)blocks, 256, 0, cs>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+    const void* fn = (n_group == 8 && topk_group == 4 && topk == 8)  // the Beam / DeepSeek-V3 router
+                         ? reinterpret_cast<const void*>(beam::route_kernel<8, 4, 8>)
+                         : reinterpret_cast<const void*>(beam::route_kernel<0, 0, 0>);
+    void* args[] = {&p};
+    cudaError_t err;
+    if (flags & BEAM_OPT_PDL) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(256);
+        cfg.stream = cs;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelExC(&cfg, fn, args);
+    } else {
+        err = cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(256), args, 0, cs);
+    }
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return BEAM_ERR_CUDA;
+    }
     return BEAM_OK;
+}
+
+beam_status beam_moe_route(beam_stream_t stream, const float* logits, const float* bias, int64_t T, int E,
+                           int n_group, int topk_group, int topk, float route_scale, int32_t* topk_idx,
+                           float* topk_w) {
+    return beam_moe_route_ex(stream, logits, bias, T, E, n_group, topk_group, topk, route_scale, topk_idx, topk_w,
+                             0u);
 }
 
 static beam_status router_sigmoid_call(beam_stream_t stream, const float* z, float* s, int64_t count, int fast) {

@@ -25,6 +25,7 @@
 #include <cstdint>
 
 #include "router_sigmoid.cuh"
+#include "tma.cuh"
 
 namespace beam {
 
@@ -149,6 +150,9 @@ __global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    // with a programmatic launch the next kernel on the stream may start its
+    // own prologue now; this one reads nothing until the previous kernel is done
+    pdl_trigger();
     if (t >= p.T) return;  // whole warps leave together
     const unsigned full = 0xFFFFFFFFu;
     const int n_group = NG ? NG : p.n_group;
@@ -157,12 +161,13 @@ __global__ void __launch_bounds__(256, 5) route_kernel(const RouteParams p) {
     const int lpg = 32 / n_group;  // lanes per group (a power of two)
     const int my_group = lane / lpg;
 
+    const SigmoidLane lt = sigmoid_lane_table();  // a constant table: readable before the wait
+    pdl_wait();
     const float4* z4 = reinterpret_cast<const float4*>(p.logits + t * kRouteExperts + 8 * lane);
     const float4* b4 = reinterpret_cast<const float4*>(p.bias + 8 * lane);
     const float4 za = __ldg(z4), zb = __ldg(z4 + 1), ba = __ldg(b4), bb = __ldg(b4 + 1);
     const float z[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
     const float bias[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
-    const SigmoidLane lt = sigmoid_lane_table();
     float4* zrow = reinterpret_cast<float4*>(&zs[warp][8 * lane]);
     zrow[0] = za;
     zrow[1] = zb;

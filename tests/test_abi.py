@@ -183,6 +183,13 @@ def test_route_and_scaled_combine_argument_errors(lib):
     assert route(w=I + 16) == _lib.BEAM_ERR_ALIAS    # weights over the ids
     assert route(i=Z + 64) == _lib.BEAM_ERR_ALIAS    # ids inside the logits
 
+    def route_ex(flags, T=4):
+        return lib.beam_moe_route_ex(None, Z, Bi, T, 256, 8, 4, 8, 2.5, I, W, flags)
+
+    assert route_ex(_lib.BEAM_OPT_FORCE_EXACT_SUM) == _lib.BEAM_ERR_ARG  # only BEAM_OPT_PDL
+    assert route_ex(0x80) == _lib.BEAM_ERR_ARG
+    assert route_ex(_lib.BEAM_OPT_PDL, T=0) == _lib.BEAM_OK
+
     def scaled(sc=2.5, **kw):
         args = dict(h=A, e=A + (1 << 32), w=A + (5 << 32), pw=A + (2 << 32), qw=A + (3 << 32),
                     y=A + (4 << 32))

@@ -487,6 +487,44 @@ def test_routing_matches_the_oracle(ng, tg, k, scale):
                    f"route ng={ng} tg={tg} k={k}")
 
 
+def test_routing_chain_with_pdl_in_a_cuda_graph():
+    """Eight routings back to back as programmatic dependent launches in one CUDA
+    graph, each writing its weights over the first logits of the next one: every
+    layer's ids and weights equal the oracle run in sequence, so no launch read
+    its logits before the launch in front of it had written them."""
+    T, L = 64, 8
+    rng = np.random.default_rng(77)
+    z = [(rng.standard_normal((T, 256)) * 2).astype(np.float32) for _ in range(L + 1)]
+    b = (rng.standard_normal(256) * 0.05).astype(np.float32)
+    dz = [torch.from_numpy(t).to(DEV) for t in z]
+    db = torch.from_numpy(b).to(DEV)
+    idx = [torch.empty((T, 8), dtype=torch.int32, device=DEV) for _ in range(L)]
+    w = [dz[i + 1].view(-1)[:T * 8].view(T, 8) for i in range(L)]  # layer i's weights: layer i+1's logits
+    stream = torch.cuda.Stream()
+
+    def run():
+        for i in range(L):
+            snr.moe_route(dz[i], db, idx=idx[i], w=w[i], stream=stream, pdl=True)
+
+    with torch.cuda.stream(stream):
+        run()
+    torch.cuda.synchronize()
+    for t, d in zip(z, dz):
+        d.copy_(torch.from_numpy(t).to(DEV))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    g.replay()
+    torch.cuda.synchronize()
+    snr.sync_status()
+    zc = [t.copy() for t in z]
+    for i in range(L):
+        idx_o, w_o = oracle.route(zc[i], b)
+        zc[i + 1].reshape(-1)[:T * 8] = w_o.reshape(-1)
+        _check_routing(idx[i].cpu().numpy(), w[i].cpu().numpy(), idx_o, w_o, f"route pdl layer {i}")
+
+
 def test_routing_with_infinite_and_extreme_logits():
     """Logits of +-inf, +-100, -95 (a subnormal sigmoid) and +-50 beside ordinary ones:
     the sigmoid saturates to exactly 1, underflows to 0 or is a subnormal, on both sides
