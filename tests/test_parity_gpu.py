@@ -487,24 +487,26 @@ def test_routing_matches_the_oracle(ng, tg, k, scale):
                    f"route ng={ng} tg={tg} k={k}")
 
 
-def test_routing_chain_with_pdl_in_a_cuda_graph():
+@pytest.mark.parametrize("ng,tg,k", [(8, 4, 8), (4, 2, 16)])
+def test_routing_chain_with_pdl_in_a_cuda_graph(ng, tg, k):
     """Eight routings back to back as programmatic dependent launches in one CUDA
     graph, each writing its weights over the first logits of the next one: every
     layer's ids and weights equal the oracle run in sequence, so no launch read
-    its logits before the launch in front of it had written them."""
+    its logits before the launch in front of it had written them. (8, 4, 8) runs
+    the compiled Beam router, (4, 2, 16) the kernel with run-time parameters."""
     T, L = 64, 8
-    rng = np.random.default_rng(77)
+    rng = np.random.default_rng(77 + k)
     z = [(rng.standard_normal((T, 256)) * 2).astype(np.float32) for _ in range(L + 1)]
     b = (rng.standard_normal(256) * 0.05).astype(np.float32)
     dz = [torch.from_numpy(t).to(DEV) for t in z]
     db = torch.from_numpy(b).to(DEV)
-    idx = [torch.empty((T, 8), dtype=torch.int32, device=DEV) for _ in range(L)]
-    w = [dz[i + 1].view(-1)[:T * 8].view(T, 8) for i in range(L)]  # layer i's weights: layer i+1's logits
+    idx = [torch.empty((T, k), dtype=torch.int32, device=DEV) for _ in range(L)]
+    w = [dz[i + 1].view(-1)[:T * k].view(T, k) for i in range(L)]  # layer i's weights: layer i+1's logits
     stream = torch.cuda.Stream()
 
     def run():
         for i in range(L):
-            snr.moe_route(dz[i], db, idx=idx[i], w=w[i], stream=stream, pdl=True)
+            snr.moe_route(dz[i], db, ng, tg, k, idx=idx[i], w=w[i], stream=stream, pdl=True)
 
     with torch.cuda.stream(stream):
         run()
@@ -520,8 +522,8 @@ def test_routing_chain_with_pdl_in_a_cuda_graph():
     snr.sync_status()
     zc = [t.copy() for t in z]
     for i in range(L):
-        idx_o, w_o = oracle.route(zc[i], b)
-        zc[i + 1].reshape(-1)[:T * 8] = w_o.reshape(-1)
+        idx_o, w_o = oracle.route(zc[i], b, ng, tg, k)
+        zc[i + 1].reshape(-1)[:T * k] = w_o.reshape(-1)
         _check_routing(idx[i].cpu().numpy(), w[i].cpu().numpy(), idx_o, w_o, f"route pdl layer {i}")
 
 
