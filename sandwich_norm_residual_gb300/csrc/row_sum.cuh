@@ -41,10 +41,13 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
     return d;
 }
 
-// Packed FP32 pairs in hand-written PTX with explicit .rn rounding: an
-// explicit rounding modifier keeps a multiply and a following add as two
-// roundings (PTX never contracts them into a fused multiply-add), which the
-// method's separately rounded FP32 products need.
+// Packed FP32 pairs in hand-written PTX with explicit .rn rounding. The
+// explicit modifier is meant to keep a multiply and a following add as two
+// roundings, yet a packed add fed by a packed product was measured to fuse into
+// an FMA on sm_103a. So a packed add here only ever takes products that are
+// exact in FP32 (squares of BF16 values), where a fused and a separately
+// rounded sum give the same bits; products that are not exact feed
+// conversions, or scalar __fadd_rn / __fsub_rn, which are never contracted.
 #define BEAM_F32X2_OP(NAME, OP)                                                                  \
     __device__ __forceinline__ float2 NAME(float2 a, float2 b) {                                 \
         float2 d;                                                                                \
