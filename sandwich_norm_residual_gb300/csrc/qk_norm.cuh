@@ -183,9 +183,18 @@ __global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
     uint4 v[4];
     load(v, hbeg);
 
-    // the q and k norm weights, one copy per warp
-    __shared__ uint4 wsm[8][32];
-    wsm[threadIdx.x >> 5][lane] = __ldg(reinterpret_cast<const uint4*>(lane < 16 ? p.qw : p.kw) + (lane & 15));
+    // the q and k norm weights widened to FP32, one copy per warp, laid out like
+    // the table below (q at 0, k at 160): 16-byte reads in distinct banks, and
+    // no unpacking per batch (SSMax 81.7 -> 80.6 us at T = 16384)
+    __shared__ __align__(16) float wsf[8][320];
+    {
+        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(lane < 16 ? p.qw : p.kw) + (lane & 15));
+        const int e = 8 * (lane & 15);
+        float* d = &wsf[threadIdx.x >> 5][(lane < 16 ? 0 : 160) + 80 * (e >> 6) + 20 * ((e >> 4) & 3) + (e & 15)];
+        const float2 w01 = bf2_to_f2(wv.x), w23 = bf2_to_f2(wv.y), w45 = bf2_to_f2(wv.z), w67 = bf2_to_f2(wv.w);
+        reinterpret_cast<float4*>(d)[0] = make_float4(w01.x, w01.y, w23.x, w23.y);
+        reinterpret_cast<float4*>(d)[1] = make_float4(w45.x, w45.y, w67.x, w67.y);
+    }
     __syncwarp();
     // RoPE: the token's table row, one per warp: lane chunk li's 16 cos at
     // 20 li, its 16 sin at 80 + 20 li (the padding puts the 16-byte reads of a
@@ -234,13 +243,15 @@ __global__ void __launch_bounds__(256, 2) qk_norm_kernel(const QKParams p) {
         }
         const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(Sr, 0x1p-7f), p.eps)));
         const float2 rv = make_float2(r, r);
-        const uint4* wp = &wsm[threadIdx.x >> 5][(is_q ? 0 : 16) + 2 * li];
-        const uint4 w0 = wp[0], w1 = wp[1], w2 = wp[8], w3 = wp[9];
-        const uint32_t ww[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
-                                 w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+        const float4* wf = reinterpret_cast<const float4*>(&wsf[threadIdx.x >> 5][(is_q ? 0 : 160) + 20 * li]);
         uint32_t n[16], o[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) n[i] = f2_to_bf2(mul2_rn(mul2_rn(bf2_to_f2(w[i]), rv), bf2_to_f2(ww[i])));
+        for (int j = 0; j < 8; ++j) {
+            const float4 wq = wf[j < 4 ? j : j + 16];
+            const int i = 2 * j;
+            n[i] = f2_to_bf2(mul2_rn(mul2_rn(bf2_to_f2(w[i]), rv), make_float2(wq.x, wq.y)));
+            n[i + 1] = f2_to_bf2(mul2_rn(mul2_rn(bf2_to_f2(w[i + 1]), rv), make_float2(wq.z, wq.w)));
+        }
         if (MODE == 0) {
             float2 cv[8], sv[8];
 #pragma unroll
