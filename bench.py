@@ -38,14 +38,14 @@ WORKLOAD = (f"layer boundary pair, T={T_TOKENS} tokens per GPU, D={D}: dense bou
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "moe": {"bytes_per_launch": 1_510_965_504 + 300_467_712, "source_sha": "fdfb284c4f3c9b13"},
-    "dense": {"bytes_per_launch": 335_662_592 + 264_134_912, "source_sha": "fdfb284c4f3c9b13"},
+    "moe": {"bytes_per_launch": 1_511_092_480 + 300_573_440, "source_sha": "b6b335c48b9cdff0"},
+    "dense": {"bytes_per_launch": 335_653_376 + 264_058_624, "source_sha": "b6b335c48b9cdff0"},
 }
 
 # Routing is bound by instruction issue, not HBM: its warp-instructions per
 # launch at T = 16384 (ncu smsp__inst_executed.sum) give its issue roofline,
 # valid while the kernel source matches.
-ROUTE_ISSUE = {"warp_instructions_per_launch": 11_224_712, "source_sha": "fdfb284c4f3c9b13"}
+ROUTE_ISSUE = {"warp_instructions_per_launch": 11_224_712, "source_sha": "b6b335c48b9cdff0"}
 
 
 def kernel_source_sha() -> str:
