@@ -126,18 +126,21 @@ class NvmlClockSampler:
             self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
                 lib.nvmlDeviceGetCurrentClocksThrottleReasons
             self.lib, self.h, self.ct = lib, h, ctypes
+            mx = ctypes.c_uint(0)  # the maximum SM clock does not change: read it once
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:  # NVML_CLOCK_SM
+                return
+            self.max_mhz = float(mx.value)
             self.ok = self._poll() is not None
         except (OSError, AttributeError):
             self.ok = False
 
     def _poll(self):
         ct = self.ct
-        mhz, mx, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        mhz, rs = ct.c_uint(0), ct.c_ulonglong(0)
         if (self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) != 0 or  # NVML_CLOCK_SM
-                self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx)) != 0 or
                 self.reasons_fn(self.h, ct.byref(rs)) != 0):
             return None
-        return float(mhz.value), float(mx.value), int(rs.value)
+        return float(mhz.value), self.max_mhz, int(rs.value)
 
     def _run(self):
         while not self._stop.is_set():
